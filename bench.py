@@ -1,0 +1,391 @@
+"""Decode benchmark: weight-absorbed paged MLA decode on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config dsv3|tiny|long_skewed|spec_q4|fp8_kv]
+
+A step is one whole decode (split-KV main kernel + LSE combine) over one
+resident batch of the DeepSeek-V3-shaped workload (B=64 requests, q_len=1,
+H=128, kv_lora_rank 512 + rope 64, L ~ U[1024, 4096], page 64, shuffled
+16384-page pool, seed 0).  L2 is flushed (a write of 2x the L2 size) between
+steps, outside the timed events.  Rank 0 prints one JSON line.
+
+--impl reference times the float64 CPU oracle (the only reference this
+decode has) on the host cores, same workload and metric.
+"""
+
+from __future__ import annotations
+
+import os
+
+# BLAS threads for the CPU oracle: every host core (set before numpy loads)
+_CORES = os.cpu_count() or 1
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import re  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_mla_decode_08_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MLA decode tokens/s, KV HBM GB/s and tensor TFLOPS as % of roofline, 1×GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+MAIN_KERNEL_SOURCES = ["mla_simt.cu", "mla_internal.h"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in MAIN_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_mla_decode_08_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config_name):
+    """DRAM bytes per launch of the main kernel from the committed ncu summary,
+    if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"mla_main_{config_name}_ncu.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    hsh = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
+    if not m or not hsh or hsh.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+def workload_desc(w):
+    return {
+        "workload": f"{w.name}: {w.meta.get('desc', '')}",
+        "batch": w.batch, "q_len": w.q_len, "num_heads": w.num_heads, "kv_dim": 576,
+        "kv_lora_rank": 512, "page_size": w.page_size, "kv_dtype": w.kv_dtype,
+        "pool_pages": w.num_pages, "seed": w.meta.get("seed", 0),
+        "kv_tokens": int(w.seq_lens.sum()),
+        "l2": "flushed between steps (write of 2x L2, outside the timed events)",
+        "kv_cache": "resident in HBM (persistent state, like weights)",
+    }
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.t0 = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t0 = time.time()
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append(parts)
+        return rows
+
+    @staticmethod
+    def summarize(rows, peaks):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": peaks.get("sm_max_mhz"), "reasons": ["no samples"],
+                    "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+
+def time_oracle(w, budget_s=10.0, max_s=30.0):
+    """The float64 oracle as it stands, on the host cores; whole workload
+    passes repeated until ``budget_s`` (request-sized steps, bounded)."""
+    from oracle import mla_ref as O
+    t0 = time.perf_counter()
+    rows = 0
+    passes = 0
+    b = 0
+    while True:
+        O.mla_decode(w.q_nope_bits, w.q_pe_bits, w.kv_bits, w.kv_dtype, w.block_table, w.seq_lens,
+                     w.q_len, w.page_size, w.scale, w.k_scale, requests=[b])
+        rows += w.q_len
+        b += 1
+        if b == w.batch:
+            b = 0
+            passes += 1
+        el = time.perf_counter() - t0
+        if (el >= budget_s and (passes >= 1 or el >= max_s)) or el >= max_s:
+            break
+    return rows / el, el, rows
+
+
+def reference_arm(args, w, rank):
+    if rank != 0:
+        return
+    st = W.workload_stats(w)
+    from oracle import mla_ref as O
+    # a step = one bounded sample of the workload: the first requests whose
+    # KV adds up to ~1/8 of the batch (keeps K steps within a few minutes)
+    target = st["kv_tokens"] / 8
+    reqs, acc = [], 0
+    for b in range(w.batch):
+        reqs.append(b)
+        acc += int(w.seq_lens[b])
+        if acc >= target:
+            break
+    def step():
+        O.mla_decode(w.q_nope_bits, w.q_pe_bits, w.kv_bits, w.kv_dtype, w.block_table, w.seq_lens,
+                     w.q_len, w.page_size, w.scale, w.k_scale, requests=reqs)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    toks = len(reqs) * w.q_len * args.steps
+    value = toks / el
+    sample = f"requests 0..{reqs[-1]} of the workload ({acc} KV tokens) per step, float64 NumPy oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_desc(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _CORES, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def our_arm(args, w, rank, world):
+    import torch
+    from paged_mla_decode_08_gb300 import binding as B
+    from paged_mla_decode_08_gb300 import runner as R
+    from paged_mla_decode_08_gb300.build import build
+
+    build()
+    B.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl", device_id=dev)
+        dist = dist_mod
+    peaks, peaks_kind = load_peaks()
+    st = W.workload_stats(w)
+    db = R.upload(w, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    launches_per_step = 1 + (1 if db.plan.num_partial_slots > 0 else 0)
+
+    def step():
+        R.decode_main(db, stream)
+        R.decode_combine(db, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    # soak: keep the GPU busy with the same step so the clock sampler sees a
+    # steady state even when K is small
+    sampler = ClockSampler(dev.index)
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:
+        for _ in range(50):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        R.decode_main(db, stream)
+        ev[k][1].record(stream)
+        R.decode_combine(db, stream)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    clock_rows = sampler.stop()
+    main_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    comb_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    tot_s = sum(step_ms) / 1e3
+    if dist:
+        t = torch.tensor([tot_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_s = float(t.item())
+    tokens = st["tokens"] * K * world
+    value = tokens / tot_s
+    ms_per_step = tot_s * 1e3 / K
+
+    # ---- e2e: host buffers in, results back to the host, copies timed
+    e2e = e2e_measure(db, w, dev, stream, max(3, min(K, 200)))
+
+    if rank != 0:
+        return
+    main_avg_s = statistics.mean(main_ms) / 1e3
+    step_avg_s = statistics.mean(step_ms) / 1e3
+    hbm_peak = float(peaks["hbm_gbs"])
+    tc_peak = float(peaks["bf16_tflops"])
+    t_hbm = st["alg_bytes"] / (hbm_peak * 1e9)
+    t_tc = st["flops"] / (tc_peak * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    if bound == "hbm":
+        achieved = st["alg_bytes"] / main_avg_s / 1e9
+        peak, unit = hbm_peak, "GB/s"
+    else:
+        achieved = st["flops"] / main_avg_s / 1e12
+        peak, unit = tc_peak, "TFLOP/s"
+    cpu_v, cpu_el, cpu_rows = time_oracle(w, budget_s=args.cpu_seconds)
+    clocks = ClockSampler.summarize(clock_rows, peaks)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3-kv/bf16-mma",
+        "data": "synthetic", "config": workload_desc(w),
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                     "kernel": "main split-KV decode kernel", "peak_kind": peaks_kind,
+                     "alg_bytes_per_launch": st["alg_bytes"], "alg_flops_per_launch": st["flops"]},
+        "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": _CORES, "kind": "oracle",
+                         "sample": f"whole-request float64 oracle passes over the same workload, "
+                                   f"{cpu_rows} query tokens in {cpu_el:.1f} s"},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "kv_gbs": st["kv_bytes"] / step_avg_s / 1e9,
+        "tflops": st["flops"] / step_avg_s / 1e12,
+        "step_roofline_frac": max(t_hbm, t_tc) / step_avg_s,
+        "main_kernel_frac_of_roofline_time": max(t_hbm, t_tc) / main_avg_s,
+        "main_ms": statistics.mean(main_ms), "combine_ms": statistics.mean(comb_ms),
+        "main_ms_median": statistics.median(main_ms),
+        "t_roof_us": {"hbm": t_hbm * 1e6, "tensor": t_tc * 1e6},
+        "wall_s_timed_loop": wall,
+        "segments": int(len(db.plan.segments())), "partial_slots": db.plan.num_partial_slots,
+        "kernel_source_sha": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def e2e_measure(db, w, dev, stream, K):
+    """The same decode through the public API starting from pinned host
+    buffers: per step, copy the query, block table and lengths in, decode,
+    copy out and lse back, wait for them on the host."""
+    import torch
+    from paged_mla_decode_08_gb300 import runner as R
+    hq = db.q_nope.cpu().pin_memory()
+    hp = db.q_pe.cpu().pin_memory()
+    hbt = db.block_table.cpu().pin_memory()
+    hsl = db.seq_lens.cpu().pin_memory()
+    ho = torch.empty(db.out.shape, dtype=db.out.dtype).pin_memory()
+    hl = torch.empty(db.lse.shape, dtype=db.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hp, hbt, hsl))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl))
+
+    def one():
+        db.q_nope.copy_(hq, non_blocking=True)
+        db.q_pe.copy_(hp, non_blocking=True)
+        db.block_table.copy_(hbt, non_blocking=True)
+        db.seq_lens.copy_(hsl, non_blocking=True)
+        R.decode(db, stream)
+        ho.copy_(db.out, non_blocking=True)
+        hl.copy_(db.lse, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    for _ in range(3):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        one()
+    el = time.perf_counter() - t0
+    return {"value": w.num_tokens * K / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K,
+            "note": "host-synchronous per step, L2 not flushed; KV cache resident in HBM"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="dsv3", choices=list(W.CONFIGS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed steps before timing")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    # weak scaling: every rank decodes its own batch of the same shape
+    w = W.make_workload(args.config, seed=args.seed + rank)
+    if args.impl == "reference":
+        reference_arm(args, w, rank)
+        return
+    our_arm(args, w, rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) paged MLA decode library.
+ *
+ * Operation.  Weight-absorbed Multi-head Latent Attention decode over a paged
+ * latent KV cache, the call the serving pages make into their decode kernels
+ * (sglang trtllm_mla_backend.py, TRTLLMMLABackend._run_decode_kernel /
+ * forward_decode; tokenspeed trtllm_mla.py, forward_decode; tokenspeed
+ * flashmla.py, FlashMLABackend.forward_decode and forward_extend).  For
+ * request b with L = seq_lens[b] cache tokens, query position i < q_len and
+ * head h (row t = b*q_len + i of the query):
+ *
+ *   visible keys   V = L - q_len + 1 + i          (bottom-right causal)
+ *   cache row j    kv_pages[block_table[b][j / page_size]][j % page_size]
+ *                  (576 wide: 512 latent c_kv, then 64 rotary k_pe)
+ *   score          s_j = scale * kf * (q_nope[t,h,:] . c_kv_j + q_pe[t,h,:] . k_pe_j)
+ *   out[t,h,:]     = kf * sum_{j<V} softmax(s)_j c_kv_j          (512 wide)
+ *   lse[t,h]       = ln sum_{j<V} exp(s_j)                       (natural log)
+ *
+ * with kf = k_scale for an e4m3 cache and 1 for bf16 (tokenspeed
+ * trtllm_mla.py, forward_decode: bmm1_scale = k_scale * layer.scaling; sglang
+ * _compute_decode_bmm1_scale: k_scale applies to an FP8 cache only).  Rows
+ * with V <= 0 give out = 0 and lse = -inf (sglang forward_extend: zero-KV rows
+ * are forced to out=0, lse=-inf so a later merge ignores them).
+ *
+ * Work is split in two calls, as the pages plan (get_mla_metadata /
+ * init_forward_metadata) before they run:
+ *   1. mla_decode_plan   host, once per batch shape: split-KV schedule and
+ *                        the workspace size it needs.
+ *   2. mla_decode        device, asynchronous on the caller's stream: the
+ *                        split-KV main kernel, then (if any request was split)
+ *                        the LSE combine kernel.
+ *
+ * Conventions for every function below.
+ *   - Return 0 on success or a negative MLA_ERR_* code; the message of the
+ *     last failure on the calling thread is mla_decode_last_error_string().
+ *   - Pointers marked "device" must be device memory of the current device;
+ *     "host" pointers are ordinary host memory.  The caller owns every buffer.
+ *   - Nothing in mla_decode allocates, frees or synchronises; all argument
+ *     errors are detected on the host before any launch.
+ *   - bf16 values are IEEE bfloat16, e4m3 values are OCP float8 e4m3fn.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_OK 0
+#define MLA_ERR_ARG (-1)           /* bad argument (pointer, size, dtype, page size) */
+#define MLA_ERR_WORKSPACE (-2)     /* workspace smaller than the plan needs */
+#define MLA_ERR_PLAN_MISMATCH (-3) /* shapes differ from the ones planned for */
+#define MLA_ERR_CUDA (-4)          /* a CUDA runtime call or launch failed */
+#define MLA_ERR_UNSUPPORTED (-5)   /* device is not sm_103 or lacks a feature */
+
+#define MLA_KV_BF16 0
+#define MLA_KV_E4M3 1
+
+#define MLA_KV_LORA_RANK 512
+#define MLA_ROPE_DIM 64
+#define MLA_KV_DIM 576
+
+/* Opaque host object holding one split-KV schedule.  Created by
+ * mla_decode_plan, released by mla_plan_destroy; read-only afterwards, so one
+ * plan may serve concurrent mla_decode calls. */
+typedef struct mla_plan mla_plan;
+
+/*
+ * Plan the split-KV schedule of one decode batch (the role of FlashMLA's
+ * get_mla_metadata(seq_lens, num_heads * q_len, 1) in tokenspeed flashmla.py,
+ * FlashMLABackend._init_decode_metadata: tile-scheduler metadata plus
+ * num_splits[batch + 1]).
+ *
+ *   seq_lens_host  host int32[batch]: cache tokens per request, including the
+ *                  q_len new tokens; 0 allowed.  Only read during the call.
+ *   batch          >= 1 requests.
+ *   page_size      32 or 64 tokens per cache page (the pages accept only
+ *                  these: tokenspeed trtllm_mla.py, TRTLLMMLABackend.__init__).
+ *   num_heads      query heads H >= 1; num_heads * q_len <= 128.
+ *   q_len          query tokens per request, >= 1 (q_len > 1: speculative
+ *                  verify / draft decode with the causal rule above).
+ *   num_sms        SMs to schedule for; 0 = query the current device.
+ *   plan_out       receives the new plan (caller frees with mla_plan_destroy).
+ *   workspace_bytes_out  receives the device workspace size mla_decode needs
+ *                  (0 when no request is split).
+ *
+ * The plan may also be made from upper bounds of the lengths: mla_decode
+ * masks with the device seq_lens it is given, so a request that turns out
+ * shorter only skips work (keys beyond the planned length are not visited).
+ * Errors: MLA_ERR_ARG, MLA_ERR_CUDA (device query).
+ */
+int mla_decode_plan(const int32_t* seq_lens_host, int batch, int page_size, int num_heads,
+                    int q_len, int num_sms, mla_plan** plan_out, size_t* workspace_bytes_out);
+
+/* Release a plan (NULL is ignored). */
+void mla_plan_destroy(mla_plan* plan);
+
+/*
+ * Run the decode on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *
+ *   plan          from mla_decode_plan.
+ *   q_nope        device bf16 [num_tokens, num_heads, 512], row-major; the
+ *                 absorbed no-PE query (num_tokens = batch * q_len,
+ *                 request-major then query position).
+ *   q_pe          device bf16 [num_tokens, num_heads, 64], row-major.
+ *   num_tokens, num_heads, page_size
+ *                 must equal the plan's batch * q_len, num_heads and
+ *                 page_size, else MLA_ERR_PLAN_MISMATCH (the pages re-plan
+ *                 when the batch outgrew the plan: sglang forward_decode).
+ *   kv_pages      device [num_pages, page_size, 576], row-major, element
+ *                 type kv_dtype (MLA_KV_BF16 or MLA_KV_E4M3); 16-byte aligned.
+ *   num_pages     pages in the pool (> 0).
+ *   block_table   device int32 [batch, bt_stride], physical page ids; entries
+ *                 past ceil(seq_len / page_size) are never read, so any
+ *                 padding value (-1, 0, ...) is fine.  bt_stride must cover
+ *                 the longest planned request.
+ *   seq_lens      device int32 [batch]; lengths used for masking (see plan).
+ *   scale         softmax scale, 1/sqrt(192) for DeepSeek-V3 shapes.
+ *   k_scale       per-tensor dequantisation scale of an e4m3 cache (finite,
+ *                 > 0); ignored for a bf16 cache, as the pages ignore a
+ *                 checkpoint k_scale there (sglang _compute_decode_bmm1_scale).
+ *   out           device bf16 [num_tokens, num_heads, 512]; fully written.
+ *   lse           device fp32 [num_tokens, num_heads]; fully written.
+ *   workspace     device scratch of >= the planned size, 256-byte aligned
+ *                 (may be NULL when the planned size is 0).  No initial
+ *                 contents are needed and none are kept between calls;
+ *                 calls that overlap on the GPU must not share it.
+ *
+ * Errors: MLA_ERR_ARG, MLA_ERR_PLAN_MISMATCH, MLA_ERR_WORKSPACE,
+ * MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA (launch failure).  Kernel-side faults
+ * surface as usual through the CUDA stream.
+ */
+int mla_decode(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_tokens,
+               int num_heads, const void* kv_pages, int kv_dtype, int64_t num_pages,
+               int page_size, const int32_t* block_table, int bt_stride,
+               const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The two launches of mla_decode, exposed separately so callers (and the
+ * benchmark) can time or interleave them.  mla_decode == mla_decode_main
+ * followed by mla_decode_combine on the same stream, with the same
+ * arguments.  mla_decode_main writes the rows of unsplit requests to
+ * out/lse and per-split partial results into the workspace;
+ * mla_decode_combine merges the partials of split requests by their
+ * log-sum-exp (lse = ln sum_k e^{lse_k}, out = sum_k e^{lse_k - lse} out_k;
+ * splits with lse = -inf weigh nothing) and is a no-op without splits.
+ */
+int mla_decode_main(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_tokens,
+                    int num_heads, const void* kv_pages, int kv_dtype, int64_t num_pages,
+                    int page_size, const int32_t* block_table, int bt_stride,
+                    const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                    void* workspace, size_t workspace_bytes, void* stream);
+int mla_decode_combine(const mla_plan* plan, void* out, float* lse, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* ---- plan inspection (host only; used by tests and tools) ---- */
+
+/* Device workspace bytes the plan needs. */
+size_t mla_plan_workspace_bytes(const mla_plan* plan);
+/* Workers (persistent CTA pairs) the plan schedules for. */
+int mla_plan_num_workers(const mla_plan* plan);
+/* Number of segments (work items).  A segment is one contiguous run of
+ * 64-token tiles of one request, processed by one worker. */
+int mla_plan_num_segments(const mla_plan* plan);
+/* Copy the segments into host int32 out[5 * capacity] as
+ * (worker, request, tile_begin, tile_end, partial_slot) tuples in execution
+ * order; partial_slot = -1 when the request has a single segment and is
+ * written directly.  Returns the number copied or MLA_ERR_ARG. */
+int mla_plan_get_segments(const mla_plan* plan, int32_t* out, int capacity);
+/* Number of partial-result slots in the workspace (sum of the split counts
+ * of split requests). */
+int mla_plan_num_partial_slots(const mla_plan* plan);
+
+/* Planner constants: tokens per tile, per-segment overhead charged in tiles,
+ * shortest piece a split request is cut into (in tiles). */
+void mla_planner_constants(int* tile_tokens, int* segment_overhead_tiles, int* min_split_tiles);
+
+/* Message of the last failure on the calling thread ("" if none). */
+const char* mla_decode_last_error_string(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int mla_decode_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

@@ -1,0 +1,182 @@
+"""Thin ctypes binding of libmladecode.so (the C ABI in include/mla_decode.h).
+
+Argument marshalling only: every step of the decode runs in the library's
+CUDA kernels.  Torch tensors are accepted for convenience and are only used
+for their device pointers and the current CUDA stream.  There is no fallback:
+if the library is missing, loading fails loudly.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+from .build import LIB
+
+MLA_OK = 0
+MLA_ERR_ARG = -1
+MLA_ERR_WORKSPACE = -2
+MLA_ERR_PLAN_MISMATCH = -3
+MLA_ERR_CUDA = -4
+MLA_ERR_UNSUPPORTED = -5
+MLA_KV_BF16 = 0
+MLA_KV_E4M3 = 1
+
+# Every symbol the header declares, with its ctypes signature.
+_c_int, _c_size, _vp, _i32p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)
+_DECODE_ARGS = [_vp, _vp, _vp, _c_int, _c_int, _vp, _c_int, ctypes.c_int64, _c_int, _vp, _c_int, _vp,
+                ctypes.c_float, ctypes.c_float, _vp, _vp, _vp, _c_size, _vp]
+SIGNATURES = {
+    "mla_decode_plan": (_c_int, [_i32p, _c_int, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_vp),
+                                 ctypes.POINTER(_c_size)]),
+    "mla_plan_destroy": (None, [_vp]),
+    "mla_decode": (_c_int, _DECODE_ARGS),
+    "mla_decode_main": (_c_int, _DECODE_ARGS),
+    "mla_decode_combine": (_c_int, [_vp, _vp, _vp, _vp, _c_size, _vp]),
+    "mla_plan_workspace_bytes": (_c_size, [_vp]),
+    "mla_plan_num_workers": (_c_int, [_vp]),
+    "mla_plan_num_segments": (_c_int, [_vp]),
+    "mla_plan_get_segments": (_c_int, [_vp, _i32p, _c_int]),
+    "mla_plan_num_partial_slots": (_c_int, [_vp]),
+    "mla_planner_constants": (None, [ctypes.POINTER(_c_int)] * 3),
+    "mla_decode_last_error_string": (ctypes.c_char_p, []),
+    "mla_decode_version": (_c_int, []),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class MlaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"MLA error {code}: {msg}")
+        self.code = code
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the library (built by build.build()); raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB
+    if not os.path.exists(p):
+        raise RuntimeError(f"libmladecode.so not built ({p}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != MLA_OK:
+        raise MlaError(rc, load().mla_decode_last_error_string().decode())
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Plan:
+    """Owner of an ``mla_plan*``; destroyed with the object."""
+
+    def __init__(self, handle: int, workspace_bytes: int, batch: int, page_size: int,
+                 num_heads: int, q_len: int):
+        self.handle = handle
+        self.workspace_bytes = workspace_bytes
+        self.batch, self.page_size, self.num_heads, self.q_len = batch, page_size, num_heads, q_len
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.mla_plan_destroy(self.handle)
+            self.handle = None
+
+    @property
+    def num_workers(self) -> int:
+        return load().mla_plan_num_workers(self.handle)
+
+    @property
+    def num_partial_slots(self) -> int:
+        return load().mla_plan_num_partial_slots(self.handle)
+
+    def segments(self) -> np.ndarray:
+        """(worker, request, tile_begin, tile_end, partial_slot) rows."""
+        lib = load()
+        n = lib.mla_plan_num_segments(self.handle)
+        buf = np.zeros(5 * n, dtype=np.int32)
+        got = lib.mla_plan_get_segments(self.handle, buf.ctypes.data_as(_i32p), n)
+        if got < 0:
+            _check(got)
+        return buf.reshape(n, 5)
+
+
+def mla_decode_plan(seq_lens_host, page_size: int, num_heads: int, q_len: int = 1,
+                    num_sms: int = 0) -> Plan:
+    lib = load()
+    lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+    handle = _vp()
+    ws = _c_size()
+    _check(lib.mla_decode_plan(lens.ctypes.data_as(_i32p), int(lens.shape[0]), page_size, num_heads,
+                               q_len, num_sms, ctypes.byref(handle), ctypes.byref(ws)))
+    return Plan(handle.value, ws.value, int(lens.shape[0]), page_size, num_heads, q_len)
+
+
+def _decode_args(plan, q_nope, q_pe, kv_pages, kv_dtype, block_table, seq_lens, scale, k_scale,
+                 out, lse, workspace, workspace_bytes, stream):
+    num_pages = kv_pages.shape[0]
+    page_size = kv_pages.shape[1]
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return (plan.handle, _ptr(q_nope), _ptr(q_pe), int(q_nope.shape[0]), int(q_nope.shape[1]),
+            _ptr(kv_pages), kv_dtype, int(num_pages), int(page_size), _ptr(block_table),
+            int(block_table.shape[1]), _ptr(seq_lens), float(scale), float(k_scale), _ptr(out), _ptr(lse),
+            _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def mla_decode(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_table, seq_lens, scale: float,
+               k_scale: float, out, lse, workspace=None, workspace_bytes=None, stream=None):
+    """Decode into ``out`` / ``lse`` (torch CUDA tensors) on ``stream``."""
+    _check(load().mla_decode(*_decode_args(plan, q_nope, q_pe, kv_pages, kv_dtype, block_table, seq_lens,
+                                           scale, k_scale, out, lse, workspace, workspace_bytes, stream)))
+
+
+def mla_decode_main(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_table, seq_lens, scale: float,
+                    k_scale: float, out, lse, workspace=None, workspace_bytes=None, stream=None):
+    _check(load().mla_decode_main(*_decode_args(plan, q_nope, q_pe, kv_pages, kv_dtype, block_table,
+                                                seq_lens, scale, k_scale, out, lse, workspace,
+                                                workspace_bytes, stream)))
+
+
+def mla_decode_combine(plan: Plan, out, lse, workspace=None, workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().mla_decode_combine(plan.handle, _ptr(out), _ptr(lse), _ptr(workspace),
+                                     int(workspace_bytes), _stream(stream)))
+
+
+def mla_planner_constants():
+    a, b, c = _c_int(), _c_int(), _c_int()
+    load().mla_planner_constants(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+    return a.value, b.value, c.value
+
+
+def mla_decode_version() -> int:
+    return load().mla_decode_version()

@@ -1,0 +1,231 @@
+// C ABI shim: argument validation, plan handling and kernel launches.
+// Every argument error is caught here, on the host, before any launch.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "../../include/mla_decode.h"
+#include "mla_internal.h"
+
+namespace mla {
+cudaError_t launch_simt(const mla_plan& p, const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(const std::vector<CombineJob>& jobs, const DecodeArgs& a,
+                           cudaStream_t stream);
+}  // namespace mla
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return MLA_OK;
+}
+
+// Per-device capability cache: 1 = sm_103, -1 = other, 0 = unknown.
+int g_dev_ok[64];
+int g_dev_sms[64];
+std::mutex g_dev_mu;
+
+int check_device(int* sms_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(MLA_ERR_UNSUPPORTED, "device index out of range");
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev_ok[dev] == 0) {
+    int maj = 0, min = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return fail(MLA_ERR_CUDA, "cudaDeviceGetAttribute failed");
+    g_dev_ok[dev] = (maj == 10 && min == 3) ? 1 : -1;
+    g_dev_sms[dev] = sms;
+  }
+  if (g_dev_ok[dev] != 1)
+    return fail(MLA_ERR_UNSUPPORTED, "this library holds sm_103a code only (GB300 class GPU required)");
+  if (sms_out) *sms_out = g_dev_sms[dev];
+  return MLA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Prepared {
+  mla::DecodeArgs args;
+};
+
+int prepare(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_tokens, int num_heads,
+            const void* kv_pages, int kv_dtype, int64_t num_pages, int page_size,
+            const int32_t* block_table, int bt_stride, const int32_t* seq_lens, float scale,
+            float k_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+            Prepared* pr) {
+  if (!plan) return fail(MLA_ERR_ARG, "plan is NULL");
+  if (!q_nope || !q_pe || !kv_pages || !block_table || !seq_lens || !out || !lse)
+    return fail(MLA_ERR_ARG, "a required device pointer is NULL");
+  if (num_tokens != plan->batch * plan->q_len || num_heads != plan->num_heads ||
+      page_size != plan->page_size)
+    return fail(MLA_ERR_PLAN_MISMATCH,
+                "num_tokens / num_heads / page_size differ from the plan (re-plan for this batch)");
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_E4M3) return fail(MLA_ERR_ARG, "kv_dtype must be MLA_KV_BF16 or MLA_KV_E4M3");
+  if (num_pages <= 0) return fail(MLA_ERR_ARG, "num_pages must be > 0");
+  if (num_pages * (int64_t)page_size > INT32_MAX) return fail(MLA_ERR_ARG, "num_pages * page_size must be < 2^31");
+  if (bt_stride < 1 || bt_stride < plan->max_pages)
+    return fail(MLA_ERR_ARG, "bt_stride is smaller than the pages of the longest planned request");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(MLA_ERR_ARG, "scale must be finite and > 0");
+  if (kv_dtype == MLA_KV_E4M3 && (!(k_scale > 0.f) || !std::isfinite(k_scale)))
+    return fail(MLA_ERR_ARG, "k_scale must be finite and > 0");
+  if (!aligned(kv_pages, 16) || !aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4))
+    return fail(MLA_ERR_ARG, "q_nope, q_pe, kv_pages and out must be 16-byte aligned");
+  if (plan->ws_bytes > 0) {
+    if (!workspace || workspace_bytes < plan->ws_bytes)
+      return fail(MLA_ERR_WORKSPACE, "workspace is smaller than mla_plan_workspace_bytes(plan)");
+    if (!aligned(workspace, 256)) return fail(MLA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  }
+  const float kf = kv_dtype == MLA_KV_E4M3 ? k_scale : 1.0f;  // ignored for a bf16 cache
+  mla::DecodeArgs& a = pr->args;
+  a.q_nope = q_nope; a.q_pe = q_pe; a.kv = kv_pages;
+  a.block_table = block_table; a.seq_lens = seq_lens;
+  a.out = out; a.lse = lse;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_lse = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan->ws_lse_offset) : nullptr;
+  a.num_pages = num_pages; a.page_size = page_size; a.kv_dtype = kv_dtype; a.bt_stride = bt_stride;
+  a.batch = plan->batch; a.q_len = plan->q_len; a.num_heads = plan->num_heads; a.rows = plan->rows;
+  a.score_scale_log2 = (float)((double)scale * (double)kf * 1.4426950408889634);
+  a.out_scale = kf;
+  return MLA_OK;
+}
+
+int launch_main(const mla_plan* plan, const Prepared& pr, cudaStream_t stream) {
+  cudaError_t e = mla::launch_simt(*plan, pr.args, stream);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("main kernel launch: ") + cudaGetErrorString(e));
+  return MLA_OK;
+}
+
+int launch_combine(const mla_plan* plan, const Prepared& pr, cudaStream_t stream) {
+  cudaError_t e = mla::launch_combine(plan->jobs, pr.args, stream);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("combine launch: ") + cudaGetErrorString(e));
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_plan(const int32_t* seq_lens_host, int batch, int page_size, int num_heads, int q_len,
+                    int num_sms, mla_plan** plan_out, size_t* workspace_bytes_out) {
+  if (!plan_out) return fail(MLA_ERR_ARG, "plan_out is NULL");
+  *plan_out = nullptr;
+  if (num_sms < 0) return fail(MLA_ERR_ARG, "num_sms must be >= 0");
+  if (num_sms == 0) {
+    int rc = check_device(&num_sms);
+    if (rc != MLA_OK) return rc;
+  }
+  mla_plan* p = new (std::nothrow) mla_plan();
+  if (!p) return fail(MLA_ERR_ARG, "out of host memory");
+  const char* msg = "";
+  int rc = mla::build_plan(seq_lens_host, batch, page_size, num_heads, q_len, num_sms, p, &msg);
+  if (rc != MLA_OK) { delete p; return fail(rc, msg); }
+  if (p->segs.size() > (size_t)mla::kSegCapLarge || p->jobs.size() > (size_t)mla::kJobCapLarge) {
+    delete p;
+    return fail(MLA_ERR_ARG, "batch too large: the schedule exceeds one launch's segment capacity");
+  }
+  *plan_out = p;
+  if (workspace_bytes_out) *workspace_bytes_out = p->ws_bytes;
+  return ok();
+}
+
+void mla_plan_destroy(mla_plan* plan) { delete plan; }
+
+int mla_decode_main(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_tokens, int num_heads,
+                    const void* kv_pages, int kv_dtype, int64_t num_pages, int page_size,
+                    const int32_t* block_table, int bt_stride, const int32_t* seq_lens, float scale,
+                    float k_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  Prepared pr;
+  int rc = prepare(plan, q_nope, q_pe, num_tokens, num_heads, kv_pages, kv_dtype, num_pages, page_size,
+                   block_table, bt_stride, seq_lens, scale, k_scale, out, lse, workspace, workspace_bytes, &pr);
+  if (rc != MLA_OK) return rc;
+  rc = check_device(nullptr);
+  if (rc != MLA_OK) return rc;
+  rc = launch_main(plan, pr, static_cast<cudaStream_t>(stream));
+  return rc == MLA_OK ? ok() : rc;
+}
+
+int mla_decode_combine(const mla_plan* plan, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  if (!plan) return fail(MLA_ERR_ARG, "plan is NULL");
+  if (plan->jobs.empty()) return ok();
+  if (!out || !lse) return fail(MLA_ERR_ARG, "out / lse is NULL");
+  if (!workspace || workspace_bytes < plan->ws_bytes)
+    return fail(MLA_ERR_WORKSPACE, "workspace is smaller than mla_plan_workspace_bytes(plan)");
+  if (!aligned(workspace, 256)) return fail(MLA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  int rc = check_device(nullptr);
+  if (rc != MLA_OK) return rc;
+  Prepared pr;
+  std::memset(&pr, 0, sizeof(pr));
+  mla::DecodeArgs& a = pr.args;
+  a.out = out; a.lse = lse;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan->ws_lse_offset);
+  a.batch = plan->batch; a.q_len = plan->q_len; a.num_heads = plan->num_heads; a.rows = plan->rows;
+  rc = launch_combine(plan, pr, static_cast<cudaStream_t>(stream));
+  return rc == MLA_OK ? ok() : rc;
+}
+
+int mla_decode(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_tokens, int num_heads,
+               const void* kv_pages, int kv_dtype, int64_t num_pages, int page_size, const int32_t* block_table,
+               int bt_stride, const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  Prepared pr;
+  int rc = prepare(plan, q_nope, q_pe, num_tokens, num_heads, kv_pages, kv_dtype, num_pages, page_size,
+                   block_table, bt_stride, seq_lens, scale, k_scale, out, lse, workspace, workspace_bytes, &pr);
+  if (rc != MLA_OK) return rc;
+  rc = check_device(nullptr);
+  if (rc != MLA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = launch_main(plan, pr, s);
+  if (rc != MLA_OK) return rc;
+  rc = launch_combine(plan, pr, s);
+  return rc == MLA_OK ? ok() : rc;
+}
+
+size_t mla_plan_workspace_bytes(const mla_plan* plan) { return plan ? plan->ws_bytes : 0; }
+int mla_plan_num_workers(const mla_plan* plan) { return plan ? plan->num_workers : 0; }
+int mla_plan_num_segments(const mla_plan* plan) { return plan ? (int)plan->segs.size() : 0; }
+int mla_plan_num_partial_slots(const mla_plan* plan) { return plan ? plan->num_slots : 0; }
+
+int mla_plan_get_segments(const mla_plan* plan, int32_t* out, int capacity) {
+  if (!plan || !out || capacity < 0) return fail(MLA_ERR_ARG, "bad arguments");
+  const int n = std::min<int>(capacity, (int)plan->segs.size());
+  for (int i = 0; i < n; ++i) {
+    out[5 * i + 0] = plan->seg_worker[i];
+    out[5 * i + 1] = plan->segs[i].req;
+    out[5 * i + 2] = plan->segs[i].tile_begin;
+    out[5 * i + 3] = plan->segs[i].tile_end;
+    out[5 * i + 4] = plan->segs[i].slot;
+  }
+  return n;
+}
+
+void mla_planner_constants(int* tile_tokens, int* segment_overhead_tiles, int* min_split_tiles) {
+  if (tile_tokens) *tile_tokens = mla::kTileTokens;
+  if (segment_overhead_tiles) *segment_overhead_tiles = mla::kSegOverheadTiles;
+  if (min_split_tiles) *min_split_tiles = mla::kMinSplitTiles;
+}
+
+const char* mla_decode_last_error_string(void) { return g_last_error.c_str(); }
+
+int mla_decode_version(void) { return 100; }
+
+}  // extern "C"

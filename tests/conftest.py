@@ -8,3 +8,9 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+def pytest_sessionstart(session):
+    # The library is built in-tree (stamp-cached, a few seconds when stale).
+    from paged_mla_decode_08_gb300.build import build
+    build()

@@ -1,0 +1,113 @@
+"""C ABI on the host: the library loads without a GPU, exports every function
+include/mla_decode.h declares, and rejects bad arguments before any launch
+(no GPU is touched by these tests)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from paged_mla_decode_08_gb300 import binding as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mla_decode.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert "mla_decode_plan" in names and "mla_decode" in names
+    lib = ctypes.CDLL(B.LIB)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared but not exported"
+        assert n in B.SIGNATURES, f"{n} has no binding signature"
+
+
+def test_version_and_constants():
+    assert B.mla_decode_version() >= 100
+    assert B.mla_planner_constants() == (64, 2, 4)
+    assert B.load().mla_decode_last_error_string() is not None
+
+
+FAKE = 1 << 20  # a 256-aligned non-NULL address; never dereferenced: every
+                # case below is rejected on the host before any launch
+
+
+def call_decode(plan, **over):
+    kw = dict(q_nope=FAKE, q_pe=FAKE, num_tokens=plan.batch * plan.q_len, num_heads=plan.num_heads,
+              kv=FAKE, kv_dtype=B.MLA_KV_BF16, num_pages=100, page_size=plan.page_size, bt=FAKE,
+              bt_stride=64, seq_lens=FAKE, scale=0.07, k_scale=1.0, out=FAKE, lse=FAKE,
+              ws=FAKE, ws_bytes=plan.workspace_bytes, stream=None)
+    kw.update(over)
+    return B.load().mla_decode(plan.handle, kw["q_nope"], kw["q_pe"], kw["num_tokens"], kw["num_heads"],
+                               kw["kv"], kw["kv_dtype"], kw["num_pages"], kw["page_size"], kw["bt"],
+                               kw["bt_stride"], kw["seq_lens"], kw["scale"], kw["k_scale"], kw["out"],
+                               kw["lse"], kw["ws"], kw["ws_bytes"], kw["stream"])
+
+
+@pytest.fixture
+def split_plan():
+    p = B.mla_decode_plan([4000, 3000, 100], 64, 128, 1, num_sms=148)
+    assert p.workspace_bytes > 0
+    return p
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(num_tokens=5), B.MLA_ERR_PLAN_MISMATCH),
+    (dict(num_heads=64), B.MLA_ERR_PLAN_MISMATCH),
+    (dict(page_size=32), B.MLA_ERR_PLAN_MISMATCH),
+    (dict(kv_dtype=7), B.MLA_ERR_ARG),
+    (dict(num_pages=0), B.MLA_ERR_ARG),
+    (dict(num_pages=1 << 40), B.MLA_ERR_ARG),
+    (dict(bt_stride=10), B.MLA_ERR_ARG),
+    (dict(scale=0.0), B.MLA_ERR_ARG),
+    (dict(scale=float("nan")), B.MLA_ERR_ARG),
+    (dict(kv_dtype=B.MLA_KV_E4M3, k_scale=0.0), B.MLA_ERR_ARG),
+    (dict(kv_dtype=B.MLA_KV_E4M3, k_scale=float("inf")), B.MLA_ERR_ARG),
+    (dict(kv=FAKE + 8), B.MLA_ERR_ARG),
+    (dict(q_nope=None), B.MLA_ERR_ARG),
+    (dict(lse=None), B.MLA_ERR_ARG),
+    (dict(ws=None), B.MLA_ERR_WORKSPACE),
+    (dict(ws_bytes=100), B.MLA_ERR_WORKSPACE),
+    (dict(ws=FAKE + 128), B.MLA_ERR_WORKSPACE),
+])
+def test_decode_rejects(split_plan, over, code):
+    rc = call_decode(split_plan, **over)
+    assert rc == code, B.load().mla_decode_last_error_string()
+    assert B.load().mla_decode_last_error_string()
+
+
+def test_decode_null_plan():
+    rc = B.load().mla_decode(None, FAKE, FAKE, 1, 1, FAKE, 0, 1, 64, FAKE, 1, FAKE, 0.1, 1.0, FAKE, FAKE,
+                             None, 0, None)
+    assert rc == B.MLA_ERR_ARG
+
+
+def test_bf16_k_scale_is_ignored_not_rejected(split_plan):
+    # a bf16 cache ignores k_scale (any value passes validation); without a
+    # GPU the call then stops at the device check
+    rc = call_decode(split_plan, k_scale=0.0)
+    assert rc in (B.MLA_ERR_CUDA, B.MLA_ERR_UNSUPPORTED, B.MLA_OK)
+
+
+def test_combine_rejects_small_workspace(split_plan):
+    rc = B.load().mla_decode_combine(split_plan.handle, FAKE, FAKE, FAKE, 64, None)
+    assert rc == B.MLA_ERR_WORKSPACE
+
+
+def test_combine_without_splits_is_noop():
+    p = B.mla_decode_plan([10], 64, 16, 1, num_sms=148)
+    assert B.load().mla_decode_combine(p.handle, FAKE, FAKE, None, 0, None) == B.MLA_OK
+
+
+def test_segment_capacity_limit():
+    # more segments than one launch's parameter block holds
+    with pytest.raises(B.MlaError) as ei:
+        B.mla_decode_plan(np.full(5000, 10, dtype=np.int32), 64, 16, 1, num_sms=148)
+    assert ei.value.code == B.MLA_ERR_ARG
