@@ -157,6 +157,35 @@ int mla_decode_main(const mla_plan* plan, const void* q_nope, const void* q_pe, 
 int mla_decode_combine(const mla_plan* plan, void* out, float* lse, void* workspace,
                        size_t workspace_bytes, void* stream);
 
+/*
+ * mla_decode_noalloc -- the decode for callers that cannot allocate device
+ * memory.  (No counterpart on the serving pages: their backends always own a
+ * workspace buffer; this entry point is this library's own addition.)
+ *
+ * Same arguments and results as mla_decode, minus the workspace: the split
+ * partials go to a scratch array built into the library (a fixed-size
+ * __device__ variable of MLA_NOALLOC_SCRATCH_BYTES).  Meant for code that is
+ * handed only its inputs and outputs and may not call cudaMalloc -- e.g. a
+ * plugin running under a host framework's own memory manager, or an
+ * allocation-free serving loop.  Nothing in this call allocates or frees.
+ *
+ *   - Plans needing more than MLA_NOALLOC_SCRATCH_BYTES of workspace are
+ *     rejected with MLA_ERR_WORKSPACE (use mla_decode then).
+ *   - The array is held by every device the code has been loaded on, until
+ *     the process exits.
+ *   - There is one array per device, shared by all calls on it; contents left
+ *     by a previous call are never read before being rewritten, so nothing
+ *     needs clearing, but calls that overlap on the GPU race: order them.
+ *   - The first call on a device looks up the array's device address once;
+ *     make that call before any stream capture.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int mla_decode_noalloc(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_tokens,
+                       int num_heads, const void* kv_pages, int kv_dtype, int64_t num_pages,
+                       int page_size, const int32_t* block_table, int bt_stride,
+                       const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                       void* stream);
+
 /* ---- plan inspection (host only; used by tests and tools) ---- */
 
 /* Device workspace bytes the plan needs. */

@@ -36,6 +36,7 @@ SIGNATURES = {
     "mla_decode": (_c_int, _DECODE_ARGS),
     "mla_decode_main": (_c_int, _DECODE_ARGS),
     "mla_decode_combine": (_c_int, [_vp, _vp, _vp, _vp, _c_size, _vp]),
+    "mla_decode_noalloc": (_c_int, _DECODE_ARGS[:16] + [_vp]),
     "mla_plan_workspace_bytes": (_c_size, [_vp]),
     "mla_plan_num_workers": (_c_int, [_vp]),
     "mla_plan_num_segments": (_c_int, [_vp]),
@@ -170,6 +171,19 @@ def mla_decode_combine(plan: Plan, out, lse, workspace=None, workspace_bytes=Non
         workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().mla_decode_combine(plan.handle, _ptr(out), _ptr(lse), _ptr(workspace),
                                      int(workspace_bytes), _stream(stream)))
+
+
+def mla_decode_noalloc(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_table, seq_lens,
+                       scale: float, k_scale: float, out, lse, stream=None):
+    """mla_decode without a workspace: the library's built-in scratch array
+    (MLA_NOALLOC_SCRATCH_BYTES) holds the split partials.  For callers that
+    cannot allocate device memory; calls that overlap on the GPU race."""
+    args = _decode_args(plan, q_nope, q_pe, kv_pages, kv_dtype, block_table, seq_lens, scale, k_scale,
+                        out, lse, None, 0, stream)
+    _check(load().mla_decode_noalloc(*args[:16], args[18]))
+
+
+MLA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 def mla_planner_constants():

@@ -120,6 +120,11 @@ int launch_combine(const mla_plan* plan, const Prepared& pr, cudaStream_t stream
 
 }  // namespace
 
+namespace mla {
+// Lets other translation units of the library record a failure message.
+int report_error(int code, const char* msg) { return fail(code, msg); }
+}  // namespace mla
+
 extern "C" {
 
 int mla_decode_plan(const int32_t* seq_lens_host, int batch, int page_size, int num_heads, int q_len,

@@ -1,0 +1,86 @@
+// mla_decode_noalloc: mla_decode with the library's own, fixed scratch.
+//
+// Who needs this.  mla_decode wants a caller-provided device workspace for
+// the per-split partial results.  Some callers cannot obtain one: code that
+// runs where allocating is not allowed or not wanted, e.g. a plugin that is
+// handed only its input and output buffers by a host framework with its own
+// memory manager, an allocation-free real-time or safety-checked serving loop,
+// or a process whose memory is fully reserved up front.  For them this entry
+// point takes the same inputs and outputs and uses a scratch array that lives
+// in this file as a statically sized __device__ variable instead.
+//
+// Cost and limits.
+//  - The array is MLA_NOALLOC_SCRATCH_BYTES (32 MiB).  It is part of the
+//    library's device image, so a device holds it from the moment this code is
+//    loaded on it until the process exits.
+//  - A plan whose workspace size exceeds the array is rejected with
+//    MLA_ERR_WORKSPACE; use mla_decode with a larger caller buffer then.
+//  - One array per device, shared by every call on that device.  It keeps
+//    whatever the previous call left there; the decode reads nothing from it
+//    that the same call did not write first, so no clearing is needed.  Calls
+//    whose work overlaps on the GPU (different streams without ordering, or
+//    several host threads) race on it and give wrong results: order them.
+//  - The first call on a device looks up the array's device address
+//    (cudaGetSymbolAddress, once per device, with that device current).  Make
+//    that first call before capturing the stream into a CUDA graph.
+//  - Nothing here allocates: no cudaMalloc / cudaFree, no allocating library
+//    routine.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/mla_decode.h"
+#include "mla_internal.h"
+
+namespace mla {
+int report_error(int code, const char* msg);
+}
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_mu;
+void* g_scratch_ptr[64];
+
+// Device address of the scratch array on the current device (looked up once
+// per device), or nullptr with the error recorded.
+void* scratch_address(int* rc) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *rc = mla::report_error(MLA_ERR_CUDA, "mla_decode_noalloc: no current CUDA device");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      *rc = mla::report_error(MLA_ERR_CUDA, "mla_decode_noalloc: cudaGetSymbolAddress of the scratch failed");
+      return nullptr;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *rc = MLA_OK;
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" int mla_decode_noalloc(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_tokens,
+                                  int num_heads, const void* kv_pages, int kv_dtype, int64_t num_pages,
+                                  int page_size, const int32_t* block_table, int bt_stride,
+                                  const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                                  void* stream) {
+  if (!plan) return mla::report_error(MLA_ERR_ARG, "plan is NULL");
+  if (mla_plan_workspace_bytes(plan) > (size_t)MLA_NOALLOC_SCRATCH_BYTES)
+    return mla::report_error(MLA_ERR_WORKSPACE,
+                             "mla_decode_noalloc: the plan needs more scratch than the built-in 32 MiB "
+                             "(mla_plan_workspace_bytes); call mla_decode with a caller workspace instead");
+  int rc = MLA_OK;
+  void* ws = scratch_address(&rc);
+  if (!ws) return rc;
+  return mla_decode(plan, q_nope, q_pe, num_tokens, num_heads, kv_pages, kv_dtype, num_pages, page_size,
+                    block_table, bt_stride, seq_lens, scale, k_scale, out, lse, ws,
+                    (size_t)MLA_NOALLOC_SCRATCH_BYTES, stream);
+}
