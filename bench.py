@@ -40,7 +40,7 @@ from paged_mla_decode_08_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MLA decode tokens/s, KV HBM GB/s and tensor TFLOPS as % of roofline, 1×GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-MAIN_KERNEL_SOURCES = ["mla_simt.cu", "mla_internal.h"]
+MAIN_KERNEL_SOURCES = ["mla_sm103.cu", "sm103_ptx.cuh", "mla_internal.h"]
 
 
 def log(*a):

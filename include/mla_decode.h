@@ -208,6 +208,13 @@ int mla_plan_num_partial_slots(const mla_plan* plan);
  * shortest piece a split request is cut into (in tiles). */
 void mla_planner_constants(int* tile_tokens, int* segment_overhead_tiles, int* min_split_tiles);
 
+/* Kernel-side error word of the current device: 0, or the code of the first
+ * bounded wait that timed out inside a decode kernel since the last reset
+ * (the kernel then stopped early and its outputs are not valid).  Reading it
+ * synchronises with the device; reset != 0 clears it.  Errors: MLA_ERR_ARG,
+ * MLA_ERR_CUDA. */
+int mla_decode_device_error(int* code, int reset);
+
 /* Message of the last failure on the calling thread ("" if none). */
 const char* mla_decode_last_error_string(void);
 

@@ -43,6 +43,7 @@ SIGNATURES = {
     "mla_plan_get_segments": (_c_int, [_vp, _i32p, _c_int]),
     "mla_plan_num_partial_slots": (_c_int, [_vp]),
     "mla_planner_constants": (None, [ctypes.POINTER(_c_int)] * 3),
+    "mla_decode_device_error": (_c_int, [ctypes.POINTER(_c_int), _c_int]),
     "mla_decode_last_error_string": (ctypes.c_char_p, []),
     "mla_decode_version": (_c_int, []),
 }
@@ -190,6 +191,13 @@ def mla_planner_constants():
     a, b, c = _c_int(), _c_int(), _c_int()
     load().mla_planner_constants(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
     return a.value, b.value, c.value
+
+
+def mla_decode_device_error(reset: bool = True) -> int:
+    """Kernel-side error word (0 = no bounded wait timed out); synchronises."""
+    code = _c_int()
+    _check(load().mla_decode_device_error(ctypes.byref(code), 1 if reset else 0))
+    return code.value
 
 
 def mla_decode_version() -> int:

@@ -18,7 +18,7 @@ from paged_mla_decode_08_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-ORACLE_CACHE = {}
+from paged_mla_decode_08_gb300 import binding as B
 
 
 def oracle(w, requests=None):
@@ -54,6 +54,7 @@ def run_gpu(w, **kw):
     db = R.upload(w, **kw)
     out, lse = R.decode(db)
     torch.cuda.synchronize()
+    assert B.mla_decode_device_error() == 0, "a bounded wait timed out inside the kernel"
     return db, out, lse
 
 
