@@ -21,9 +21,10 @@
 // Shared memory: 4-stage cache-tile ring (36 KB per stage), the rope half of
 // Q (8 KB), two 32 KB score-exchange buffers written by the peer CTA.
 //
-// Warp roles (256 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer, warps 4-7 softmax / correction / epilogue (thread = query row =
-// TMEM lane), warps 2-3 idle.  Every wait is bounded: on timeout the kernel
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and
+// MMA issuer, warps 4-11 softmax / correction / epilogue (two warps per query
+// row block = TMEM lane quadrant, each owning half of a tile's keys and half
+// of the output columns), warps 2-3 spare.  Every wait is bounded: on timeout the kernel
 // records an error code in device memory, stops every role, waits for its
 // own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -43,7 +44,7 @@ namespace sm103 {
 
 using namespace mla::ptx;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;  // warps 0-3: producer, MMA, 2 spare; 4-11: softmax
 constexpr int kStages = 4;
 constexpr int kLatBox = 64 * 128;           // 64 tokens x 64 bf16 columns, 128B swizzle
 constexpr int kRopeBox = 64 * 64;           // 64 tokens x 32 bf16 columns, 64B swizzle
@@ -53,11 +54,16 @@ constexpr int OFF_KV = 0;
 constexpr int OFF_QROPE = kStages * kStageBytes;       // 128 rows x 64 B
 constexpr int OFF_XCHG = OFF_QROPE + 128 * 64;         // 2 x (128 rows x 256 B)
 constexpr int kXchgBytes = 128 * 64 * 4;
-constexpr int OFF_BAR = OFF_XCHG + 2 * kXchgBytes;
+constexpr int OFF_RED = OFF_XCHG + 2 * kXchgBytes;     // row max / row sum exchange, 4 KB
+constexpr int OFF_SINK = OFF_RED + 4 * 2 * 128 * 4;    // 2 x 256 words the peer's "read done" notes land in
+constexpr int kNoteBytes = 256 * 4;
+constexpr int OFF_BAR = OFF_SINK + 2 * kNoteBytes;
 enum Bar : int {
   B_KV_FULL = 0, B_KV_EMPTY = B_KV_FULL + kStages, B_S_FULL = B_KV_EMPTY + kStages, B_P_FULL = B_S_FULL + 2,
   B_PV_DONE = B_P_FULL + 2, B_Q_READY, B_X_FULL, B_X_EMPTY = B_X_FULL + 2, B_TAIL = B_X_EMPTY + 2, B_FINAL,
-  B_COUNT
+  B_PAIR_MAX,                 // [quad][tile parity]: the two warps of a quadrant swap row maxima
+  B_PAIR_L = B_PAIR_MAX + 8,  // [quad]: ... and row sums at a segment's end
+  B_COUNT = B_PAIR_L + 4
 };
 constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
@@ -264,20 +270,54 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& rlo, fl
 template <int CAP>
 __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, uint32_t tmem,
                                  int worker, int rank) {
-  const int row = threadIdx.x - 128;       // query row = TMEM lane
-  const int quad = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant of this warp
+  // Two warps per TMEM lane quadrant: warp (4 + q) and (8 + q) own query rows
+  // 32q..32q+31 (= TMEM lanes); `half` selects which 32 of a tile's 64 keys
+  // (and which 128 of this CTA's 256 output columns) the thread handles.
+  const int sw = (threadIdx.x >> 5) - 4;
+  const int quad = (threadIdx.x >> 5) & 3;
+  const int half = sw >> 2;
+  const int row = quad * 32 + (threadIdx.x & 31);
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   const uint32_t peer = rank ^ 1;
   const int M = a.rows;
   const bool valid_row = row < M;
   const int qi = valid_row ? row / a.num_heads : 0;  // query position of this row
-  const uint32_t xchg_local = c.sbase + OFF_XCHG;
-  const uint32_t xchg_peer = mapa(xchg_local, peer);
-  const uint32_t x_full_peer[2] = {mapa(c.bar(B_X_FULL), peer), mapa(c.bar(B_X_FULL + 1), peer)};
-  const uint32_t x_empty_peer[2] = {mapa(c.bar(B_X_EMPTY), peer), mapa(c.bar(B_X_EMPTY + 1), peer)};
-  const int swz = row & 15;
-  int j = 0;
+  // Exchange buffers, [16-byte chunk][row] so a warp's stores are contiguous.
+  // This thread's 8 chunks start at chunk 8*half.
+  const uint32_t my_off = static_cast<uint32_t>((half * 8 * 128 + row) * 16);
+  const uint32_t xchg_local = c.sbase + OFF_XCHG + my_off;
+  const uint32_t xchg_peer = mapa(c.sbase + OFF_XCHG, peer) + my_off;
+  const uint32_t x_full_peer0 = mapa(c.bar(B_X_FULL), peer), x_full_peer1 = mapa(c.bar(B_X_FULL + 1), peer);
+  const uint32_t x_empty_peer0 = mapa(c.bar(B_X_EMPTY), peer), x_empty_peer1 = mapa(c.bar(B_X_EMPTY + 1), peer);
+  const uint32_t sink_peer = mapa(c.sbase + OFF_SINK, peer) + (threadIdx.x - 128) * 4;
+  float* red_max = reinterpret_cast<float*>(c.smem + OFF_RED);      // [2 tiles][2 halves][128]
+  float* red_l = red_max + 2 * 2 * 128;                              // [2 segments][2 halves][128]
+  const float cs = a.score_scale_log2;  // raw score -> base-2 logit
+  int j = 0, nseg = 0;
   bool ok = true;
+
+  // S partial of tile jn (this thread's 32 columns) from TMEM
+  auto load_s = [&](int jn, uint32_t(&sv)[32]) -> bool {
+    const int sb = jn & 1;
+    if (!wait_bar_warp<false>(c, c.bar(B_S_FULL + sb), (jn >> 1) & 1, 0x301)) return false;
+    tc_fence_after();
+    tmem_ld32(tmem + lane_off + TM_S + 64 * sb + 32 * half, sv);
+    tmem_ld_wait(sv);
+    return true;
+  };
+  // ... and into the peer CTA's exchange buffer
+  auto send = [&](int jn, const uint32_t(&sv)[32]) -> bool {
+    const int sb = jn & 1, u = jn >> 1;
+    if (u > 0 && !wait_bar_warp<true>(c, c.bar(B_X_EMPTY + sb), (u - 1) & 1, 0x302)) return false;
+    const uint32_t dst = xchg_peer + sb * kXchgBytes;
+    const uint32_t mb = sb ? x_full_peer1 : x_full_peer0;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+      st_async_v4(dst + ch * 2048, sv[4 * ch], sv[4 * ch + 1], sv[4 * ch + 2], sv[4 * ch + 3], mb);
+    // arm the "peer has read it" phase of this buffer: 256 four-byte notes
+    if (threadIdx.x == 128) mbar_arrive_expect_tx(c.bar(B_X_EMPTY + sb), kNoteBytes);
+    return true;
+  };
 
   for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
     const Segment sg = sched.seg[s];
@@ -288,25 +328,27 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
     float m_ref = -CUDART_INF_F, l = 0.f;
 
     if (nt > 0) {
-      // ---- Q: latent half -> TMEM columns [384, 512), rope half -> smem (64B swizzle)
+      // ---- Q: latent half -> TMEM columns [384, 512) (this thread: 128 of
+      // the 256 elements), rope half -> shared memory (64B swizzle)
       {
         uint32_t r[32];
-        const uint4* src = reinterpret_cast<const uint4*>(
-            reinterpret_cast<const __nv_bfloat16*>(a.q_nope) + ((size_t)b * M + row) * kLatent + 256 * rank);
+        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q_nope) +
+                                                          ((size_t)b * M + row) * kLatent + 256 * rank + 128 * half);
 #pragma unroll
-        for (int ck = 0; ck < 4; ++ck) {
+        for (int ck = 0; ck < 2; ++ck) {
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
-            uint4 q4 = valid_row ? __ldg(src + ck * 8 + v) : make_uint4(0, 0, 0, 0);
+            const uint4 q4 = valid_row ? __ldg(src + ck * 8 + v) : make_uint4(0, 0, 0, 0);
             r[4 * v + 0] = q4.x; r[4 * v + 1] = q4.y; r[4 * v + 2] = q4.z; r[4 * v + 3] = q4.w;
           }
-          tmem_st32(tmem + lane_off + TM_Q + 32 * ck, r);
+          tmem_st32(tmem + lane_off + TM_Q + 64 * half + 32 * ck, r);
         }
-        const uint4* srp = reinterpret_cast<const uint4*>(
-            reinterpret_cast<const __nv_bfloat16*>(a.q_pe) + ((size_t)b * M + row) * kRope + 32 * rank);
+        const uint4* srp = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q_pe) +
+                                                          ((size_t)b * M + row) * kRope + 32 * rank + 16 * half);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint4 q4 = valid_row ? __ldg(srp + ch) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 2; ++i) {
+          const int ch = 2 * half + i;
+          const uint4 q4 = valid_row ? __ldg(srp + i) : make_uint4(0, 0, 0, 0);
           st_shared_v4(c.sbase + OFF_QROPE + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4), q4);
         }
         tmem_st_wait();
@@ -315,67 +357,74 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
         mbar_arrive(c.bar(B_Q_READY));
       }
 
+      uint32_t cur[32];  // own partial scores of the tile being finished
+      if (!load_s(j, cur) || !send(j, cur)) { ok = false; break; }
       for (int jj = 0; jj < nt; ++jj, ++j) {
         const int sb = j & 1;
-        const int u = j >> 1;  // use count of S buffer / exchange buffer sb
-        if (!wait_bar_warp<false>(c, c.bar(B_S_FULL + sb), u & 1, 0x301)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t s0[32], s1[32];
-        tmem_ld32(tmem + lane_off + TM_S + 64 * sb, s0);
-        tmem_ld32(tmem + lane_off + TM_S + 64 * sb + 32, s1);
-        tmem_ld_wait(s0);
-        tmem_ld_wait(s1);
-        // ---- swap partial scores with the peer CTA
-        if (u > 0 && !wait_bar_warp<true>(c, c.bar(B_X_EMPTY + sb), (u - 1) & 1, 0x302)) { ok = false; break; }
-        const uint32_t rowp = xchg_peer + sb * kXchgBytes + row * 256;
+        // ---- the next tile's exchange first, so its DSMEM transit overlaps this tile
+        uint32_t nxt[32];
+        if (jj + 1 < nt && (!load_s(j + 1, nxt) || !send(j + 1, nxt))) { ok = false; break; }
+        // ---- full scores: own partial + the peer's (its st.async bytes
+        // complete the transaction count this CTA expects per tile)
+        if (threadIdx.x == 128) mbar_arrive_expect_tx(c.bar(B_X_FULL + sb), kXchgBytes);
+        if (!wait_bar_warp<true>(c, c.bar(B_X_FULL + sb), (j >> 1) & 1, 0x303)) { ok = false; break; }
+        float x[32];
+        {
+          const uint32_t srcx = xchg_local + sb * kXchgBytes;
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          const uint32_t* src = ch < 8 ? &s0[4 * ch] : &s1[4 * (ch - 8)];
-          st_cluster_v4(rowp + ((ch ^ swz) << 4), src[0], src[1], src[2], src[3]);
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 v = ld_shared_v4(srcx + ch * 2048);
+            x[4 * ch + 0] = __uint_as_float(cur[4 * ch + 0]) + __uint_as_float(v.x);
+            x[4 * ch + 1] = __uint_as_float(cur[4 * ch + 1]) + __uint_as_float(v.y);
+            x[4 * ch + 2] = __uint_as_float(cur[4 * ch + 2]) + __uint_as_float(v.z);
+            x[4 * ch + 3] = __uint_as_float(cur[4 * ch + 3]) + __uint_as_float(v.w);
+          }
         }
-        mbar_arrive_remote(x_full_peer[sb]);
-        if (!wait_bar_warp<true>(c, c.bar(B_X_FULL + sb), u & 1, 0x303)) { ok = false; break; }
-        float x[64];
-        const uint32_t rowl = xchg_local + sb * kXchgBytes + row * 256;
+        // ---- causal / length mask (tail tiles only), row max over both
+        // halves on the raw scores (the scale is positive)
+        const int nvis = vis - ((sg.tile_begin + jj) * kTileTokens + 32 * half);
+        if (nvis < 32) {
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          const uint4 v = ld_shared_v4(rowl + ((ch ^ swz) << 4));
-          const uint32_t* mine = ch < 8 ? &s0[4 * ch] : &s1[4 * (ch - 8)];
-          x[4 * ch + 0] = __uint_as_float(mine[0]) + __uint_as_float(v.x);
-          x[4 * ch + 1] = __uint_as_float(mine[1]) + __uint_as_float(v.y);
-          x[4 * ch + 2] = __uint_as_float(mine[2]) + __uint_as_float(v.z);
-          x[4 * ch + 3] = __uint_as_float(mine[3]) + __uint_as_float(v.w);
+          for (int k = 0; k < 32; ++k) x[k] = k < nvis ? x[k] : -CUDART_INF_F;
         }
-        mbar_arrive_remote(x_empty_peer[sb]);
-        // ---- scale, causal / length mask, tile max
-        const int key0 = (sg.tile_begin + jj) * kTileTokens;
-        const int nvis = vis - key0;  // keys of this tile visible to this row
-        float mt = -CUDART_INF_F;
+        float mt;
+        {
+          float m16[16];
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          x[k] = k < nvis ? x[k] * a.score_scale_log2 : -CUDART_INF_F;
-          mt = fmaxf(mt, x[k]);
+          for (int k = 0; k < 16; ++k) m16[k] = fmaxf(x[k], x[k + 16]);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m16[k] = fmaxf(m16[k], m16[k + 8]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) m16[k] = fmaxf(m16[k], m16[k + 4]);
+          mt = fmaxf(fmaxf(m16[0], m16[2]), fmaxf(m16[1], m16[3]));
         }
+        // tell the peer its buffer is free: a 4-byte st.async whose value (the
+        // row max) depends on every word read from the buffer
+        st_async_b32(sink_peer + sb * kNoteBytes, __float_as_uint(mt), sb ? x_empty_peer1 : x_empty_peer0);
+        red_max[(sb * 2 + half) * 128 + row] = mt;
+        mbar_arrive(c.bar(B_PAIR_MAX + 2 * quad + sb));
+        if (!wait_bar_warp<false>(c, c.bar(B_PAIR_MAX + 2 * quad + sb), (j >> 1) & 1, 0x306)) { ok = false; break; }
+        mt = fmaxf(red_max[(sb * 2) * 128 + row], red_max[(sb * 2 + 1) * 128 + row]) * cs;
         // ---- O is idle once the previous tile's P.V is done
         if (jj > 0) {
           if (!wait_bar_warp<false>(c, c.bar(B_PV_DONE), (j - 1) & 1, 0x304)) { ok = false; break; }
           tc_fence_after();
         }
-        // lazy rescale: move the reference max only when it grew by more
-        // than 2^8; the TMEM traffic is done by whole warps, rows that keep
-        // their reference use factor 1
+        // lazy rescale: the reference max moves only when it grew by more than
+        // 2^8; both halves decide identically; TMEM traffic by whole warps
         const float m_new = fmaxf(m_ref, mt);
         const bool resc = m_new > m_ref + kRescaleThreshold;
-        const float alpha = resc ? exp2f(m_ref - m_new) : 1.f;  // 0 when m_ref = -inf
+        const float alpha = resc ? ex2_approx(m_ref - m_new) : 1.f;  // 0 when m_ref = -inf
         if (jj > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-          for (int ck = 0; ck < 8; ++ck) {
+          for (int ck = 0; ck < 4; ++ck) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_off + TM_O + 32 * ck, o);
+            const uint32_t addr = tmem + lane_off + TM_O + 128 * half + 32 * ck;
+            tmem_ld32(addr, o);
             tmem_ld_wait(o);
 #pragma unroll
             for (int v = 0; v < 32; ++v) o[v] = __float_as_uint(__uint_as_float(o[v]) * alpha);
-            tmem_st32(tmem + lane_off + TM_O + 32 * ck, o);
+            tmem_st32(addr, o);
           }
           tmem_st_wait();
         }
@@ -383,47 +432,58 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
           l *= alpha;
           m_ref = m_new;
         }
+        const float nm = m_ref == -CUDART_INF_F ? 0.f : -m_ref;  // all-masked rows: 2^-inf = 0
         // ---- P (bf16 pairs) over the S columns it came from
-        uint32_t pk[32];
+        uint32_t pk[16];
         float lsum = 0.f;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float p0 = x[2 * k] == -CUDART_INF_F ? 0.f : exp2f(x[2 * k] - m_ref);
-          const float p1 = x[2 * k + 1] == -CUDART_INF_F ? 0.f : exp2f(x[2 * k + 1] - m_ref);
+        for (int k = 0; k < 16; ++k) {
+          const float p0 = ex2_approx(fmaf(x[2 * k], cs, nm));
+          const float p1 = ex2_approx(fmaf(x[2 * k + 1], cs, nm));
           float r0, r1;
           pk[k] = pack_bf16(p0, p1, r0, r1);
           lsum += p0 + p1;  // l from the unrounded probabilities: exact lse
         }
         l += lsum;
-        tmem_st32(tmem + lane_off + TM_S + 64 * sb, pk);
+        tmem_st16(tmem + lane_off + TM_S + 64 * sb + 16 * half, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(c.bar(B_P_FULL + sb));
+#pragma unroll
+        for (int k = 0; k < 32; ++k) cur[k] = nxt[k];
       }
       if (!ok) break;
       if (!wait_bar_warp<false>(c, c.bar(B_PV_DONE), (j - 1) & 1, 0x305)) { ok = false; break; }
       tc_fence_after();
     }
 
-    // ---- epilogue: this CTA's 256 output columns of the row, and (rank 0) lse.
-    // TMEM is read by whole warps (only when the segment ran MMAs); stores
-    // are per row.
+    // ---- epilogue: row sum over both halves; this thread writes 128 of the
+    // CTA's 256 output columns, (rank 0, half 0) the lse.  TMEM is read by
+    // whole warps (only when the segment ran MMAs); stores are per row.
+    {
+      float* rl = red_l + (nseg & 1) * 256;
+      rl[half * 128 + row] = l;
+      mbar_arrive(c.bar(B_PAIR_L + quad));
+      if (!wait_bar_warp<false>(c, c.bar(B_PAIR_L + quad), nseg & 1, 0x307)) { ok = false; break; }
+      l = rl[row] + rl[128 + row];
+      ++nseg;
+    }
     {
       const size_t orow = (size_t)b * M + row;
       const bool live = l > 0.f;
       const float inv = live ? a.out_scale / l : 0.f;
 #pragma unroll 1
-      for (int ck = 0; ck < 8; ++ck) {
+      for (int ck = 0; ck < 4; ++ck) {
         uint32_t o[32];
         if (nt > 0) {
-          tmem_ld32(tmem + lane_off + TM_O + 32 * ck, o);
+          tmem_ld32(tmem + lane_off + TM_O + 128 * half + 32 * ck, o);
           tmem_ld_wait(o);
         }
         if (nt == 0 || !live) {
 #pragma unroll
           for (int v = 0; v < 32; ++v) o[v] = 0u;
         }
-        const int col = 256 * rank + 32 * ck;
+        const int col = 256 * rank + 128 * half + 32 * ck;
         if (!valid_row) continue;
         if (sg.slot < 0) {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * kLatent + col);
@@ -445,8 +505,8 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
                                  __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
         }
       }
-      if (rank == 0 && valid_row) {
-        const float lse = live ? (m_ref + log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
+      if (rank == 0 && half == 0 && valid_row) {
+        const float lse = live ? (m_ref + __log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
         if (sg.slot < 0) a.lse[orow] = lse;
         else a.part_lse[(size_t)sg.slot * M + row] = lse;
       }
@@ -480,14 +540,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(c.bar(B_S_FULL + i), 1);
-      mbar_init(c.bar(B_P_FULL + i), 128);
-      mbar_init(c.bar(B_X_FULL + i), 128);
-      mbar_init(c.bar(B_X_EMPTY + i), 128);
+      mbar_init(c.bar(B_P_FULL + i), 256);
+      mbar_init(c.bar(B_X_FULL + i), 1);  // own expect_tx arrival + the peer's st.async bytes
+      mbar_init(c.bar(B_X_EMPTY + i), 1);  // own expect_tx arrival + the peer's 4-byte notes
     }
     mbar_init(c.bar(B_PV_DONE), 1);
-    mbar_init(c.bar(B_Q_READY), 128);
+    mbar_init(c.bar(B_Q_READY), 256);
     mbar_init(c.bar(B_TAIL), 1);
     mbar_init(c.bar(B_FINAL), 1);
+    for (int i = 0; i < 8; ++i) mbar_init(c.bar(B_PAIR_MAX + i), 64);
+    for (int i = 0; i < 4; ++i) mbar_init(c.bar(B_PAIR_L + i), 64);
     fence_mbar_init();
     prefetch_tensormap(&tm_lat);
     prefetch_tensormap(&tm_rope);
