@@ -9,9 +9,15 @@
 // of the pages (sglang trtllm_mla_backend.py, forward_extend: fixed-up rows
 // with lse = -inf so the merge ignores them).
 //
-// One CTA of 128 threads per (job, query row): each thread owns 4 of the 512
-// output columns, reads them from every split with 16-byte loads and writes
-// 8 bytes of bf16.  Memory bound: traffic = nsplit * 2 KB + 1 KB per row.
+// Partials are chunk-major, part_o[slot][c][row] (c = 16-byte chunk of 4
+// output columns), so that the producing kernels store coalesced.  One CTA of
+// 256 threads per (job, block of 32 query rows, quarter of the 128 chunks):
+// the split weights e^{lse_s - lse} of the 32 rows go to shared memory, then
+// a warp owns 4 chunks and reads them for 32 consecutive rows (512
+// contiguous bytes per chunk and split, four independent loads in flight),
+// and the 32 x 128 bf16 result is transposed through shared memory so that
+// each output row segment is written with contiguous 16-byte stores.
+// Memory bound: nsplit * 2 KB read + 1 KB written per row.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -19,45 +25,77 @@
 
 namespace mla {
 
+constexpr int kCombRows = 32;
+constexpr int kCombChunks = 32;  // per CTA: a quarter of the 128 chunks
+
 template <int CAP>
-__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ CombineList<CAP> jobs,
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineList<CAP> jobs,
                                                       const __grid_constant__ DecodeArgs a) {
+  extern __shared__ float s_w[];  // [nsplit][32] weights (0 for -inf splits)
   const CombineJob job = jobs.job[blockIdx.x];
-  const int m = blockIdx.y;
   const int M = a.rows;
-  const float* plse = a.part_lse + (size_t)job.slot_begin * M + m;
-  float mx = -CUDART_INF_F;
-  for (int s = 0; s < job.nsplit; ++s) mx = fmaxf(mx, plse[(size_t)s * M]);
-  const size_t row = (size_t)job.req * M + m;  // == (b*q_len + i)*H + h
-  const int col = threadIdx.x * 4;
-  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + row * kLatent + col;
-  if (mx == -CUDART_INF_F) {
-    *reinterpret_cast<uint2*>(out) = make_uint2(0u, 0u);
-    if (threadIdx.x == 0) a.lse[row] = -CUDART_INF_F;
-    return;
+  const int r0 = blockIdx.y * kCombRows;
+  const int c0 = blockIdx.z * kCombChunks;
+  const int nrows = min(kCombRows, M - r0);
+  __shared__ uint2 s_out[kCombRows][kCombChunks + 1];
+
+  if (threadIdx.x < kCombRows) {
+    const int r = threadIdx.x;
+    float mx = -CUDART_INF_F, tot = 0.f;
+    const float* pl = a.part_lse + (size_t)job.slot_begin * M + r0 + r;
+    if (r < nrows) {
+      for (int s = 0; s < job.nsplit; ++s) mx = fmaxf(mx, pl[(size_t)s * M]);
+      if (mx != -CUDART_INF_F)
+        for (int s = 0; s < job.nsplit; ++s) tot += __expf(pl[(size_t)s * M] - mx);
+      if (blockIdx.z == 0) a.lse[(size_t)job.req * M + r0 + r] = tot > 0.f ? mx + __logf(tot) : -CUDART_INF_F;
+    }
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
+    for (int s = 0; s < job.nsplit; ++s) {
+      const float l = r < nrows ? pl[(size_t)s * M] : -CUDART_INF_F;
+      s_w[s * kCombRows + r] = (inv > 0.f && l != -CUDART_INF_F) ? __expf(l - mx) * inv : 0.f;
+    }
   }
-  float tot = 0.f;
-  for (int s = 0; s < job.nsplit; ++s) tot += __expf(plse[(size_t)s * M] - mx);
-  const float inv = 1.f / tot;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float* po = a.part_o + ((size_t)job.slot_begin * M + m) * kLatent + col;
-  for (int s = 0; s < job.nsplit; ++s) {
-    const float l = plse[(size_t)s * M];
-    if (l == -CUDART_INF_F) continue;
-    const float wgt = __expf(l - mx) * inv;
-    const float4 v = __ldg(reinterpret_cast<const float4*>(po + (size_t)s * M * kLatent));
-    acc.x = fmaf(wgt, v.x, acc.x);
-    acc.y = fmaf(wgt, v.y, acc.y);
-    acc.z = fmaf(wgt, v.z, acc.z);
-    acc.w = fmaf(wgt, v.w, acc.w);
+  __syncthreads();
+
+  const int r = threadIdx.x & 31;  // row within the block
+  const int cw = threadIdx.x >> 5;  // warp: chunks c0 + cw + 8k, k < 4
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (r < nrows) {
+    const float4* po = reinterpret_cast<const float4*>(a.part_o) +
+                       ((size_t)job.slot_begin * (kLatent / 4) + c0 + cw) * M + r0 + r;
+    const size_t split_stride = (size_t)(kLatent / 4) * M;
+    for (int s = 0; s < job.nsplit; ++s) {
+      const float wgt = s_w[s * kCombRows + r];
+      if (wgt == 0.f) continue;
+      float4 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = __ldg(po + s * split_stride + (size_t)(8 * k) * M);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[k].x = fmaf(wgt, v[k].x, acc[k].x);
+        acc[k].y = fmaf(wgt, v[k].y, acc[k].y);
+        acc[k].z = fmaf(wgt, v[k].z, acc[k].z);
+        acc[k].w = fmaf(wgt, v[k].w, acc[k].w);
+      }
+    }
   }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-  uint2 pk;
-  pk.x = *reinterpret_cast<uint32_t*>(&lo);
-  pk.y = *reinterpret_cast<uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(out) = pk;
-  if (threadIdx.x == 0) a.lse[row] = mx + __logf(tot);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z, acc[k].w);
+    s_out[r][cw + 8 * k] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  }
+  __syncthreads();
+  // 32 rows x 256 bytes: a half-warp writes one row segment (16 lanes x 16 B)
+  const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
+  for (int rr = hw; rr < nrows; rr += 16) {
+    const size_t row = (size_t)job.req * M + r0 + rr;
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * kLatent + 4 * c0) + l16;
+    const uint2 x0 = s_out[rr][2 * l16], x1 = s_out[rr][2 * l16 + 1];
+    *dst = make_uint4(x0.x, x0.y, x1.x, x1.y);
+  }
 }
 
 template <int CAP>
@@ -66,7 +104,12 @@ static cudaError_t launch_combine_cap(const std::vector<CombineJob>& jobs, const
   CombineList<CAP> list;
   list.num_jobs = (int32_t)jobs.size();
   for (size_t i = 0; i < jobs.size(); ++i) list.job[i] = jobs[i];
-  combine_kernel<CAP><<<dim3((unsigned)jobs.size(), (unsigned)a.rows), 128, 0, stream>>>(list, a);
+  int maxsplit = 1;
+  for (const CombineJob& j : jobs) maxsplit = j.nsplit > maxsplit ? j.nsplit : maxsplit;
+  const size_t smem = (size_t)maxsplit * kCombRows * sizeof(float);  // <= 128 splits: 16 KB
+  combine_kernel<CAP><<<dim3((unsigned)jobs.size(), (unsigned)((a.rows + kCombRows - 1) / kCombRows),
+                             (unsigned)(kLatent / 4 / kCombChunks)),
+                        256, smem, stream>>>(list, a);
   return cudaGetLastError();
 }
 

@@ -6,18 +6,22 @@
 // below is this library's own.
 //
 // Rule.  Cut every request into 64-token tiles, n_b = ceil(L_b / 64).  There
-// are W workers (one per CTA pair, W = num_sms / 2).  Each segment (a run of
-// tiles of one request on one worker) costs its tiles plus OVH = 2 tiles of
-// fixed work (query load, epilogue).  Budget per worker:
-//     cap = max(ceil((sum_b n_b + OVH * B) / W), OVH + MIN)
-// with MIN = 4.  Requests are walked in order and poured into workers in
-// order: a worker takes as many tiles of the current request as fit into its
-// remaining budget (at least MIN), a piece of fewer than MIN tiles is never
-// left behind (it stays on the current worker), and a worker whose remaining
-// room cannot hold min(left, MIN) tiles is closed.  The last worker takes
-// whatever is left.  Zero-length requests get one empty segment (it writes
-// out = 0, lse = -inf).  A request cut into k >= 2 segments gets k
-// consecutive partial slots; a single-segment request is written directly.
+// are W workers (one per CTA pair, W = num_sms / 2, at most 128).  Each
+// segment (a run of tiles of one request on one worker) costs its tiles plus
+// OVH = 2 tiles of fixed work (query load, epilogue).  With S segments,
+//     total = sum_b n_b + OVH * S,   bound(w) = ceil((w + 1) * total / W),
+// worker w is filled until the cumulative cost of everything poured so far
+// reaches bound(w).  Requests are walked in order: a request that fits into
+// the worker's remaining room goes there whole; otherwise the worker takes
+// `room` tiles of it (a worker whose room is below MIN = 4 tiles and that
+// already holds work is closed first), and if that would leave fewer than MIN
+// tiles behind it takes `left - MIN` instead (or everything when that is
+// below MIN).  Because the bounds are absolute, rounding never accumulates.
+// The last worker takes whatever is left.  S is not known before pouring:
+// the first pass assumes S = B + W - 1, the second uses the first pass's S.  Zero-length requests get
+// one empty segment (it writes out = 0, lse = -inf).  A request cut into
+// k >= 2 segments gets k consecutive partial slots; a single-segment request
+// is written directly.
 #include <algorithm>
 #include <cstdint>
 
@@ -53,38 +57,51 @@ int build_plan(const int32_t* seq_lens, int batch, int page_size, int num_heads,
     max_len = std::max<int64_t>(max_len, seq_lens[b]);
   }
   p->max_pages = (int)((max_len + page_size - 1) / page_size);
-  const int64_t cap = std::max<int64_t>((total + W - 1) / W, kSegOverheadTiles + kMinSplitTiles);
+  int64_t tiles_sum = total - (int64_t)kSegOverheadTiles * batch;
+  int64_t nsegs = (int64_t)batch + W - 1;
+  for (int pass = 0; pass < 2; ++pass) {
+  total = tiles_sum + (int64_t)kSegOverheadTiles * nsegs;
+  auto bound = [&](int w) -> int64_t { return ((int64_t)(w + 1) * total + W - 1) / W; };
 
   p->segs.clear(); p->seg_worker.clear();
   int w = 0;
-  int64_t used = 0;
-  auto close_if_full = [&]() {
-    if (used >= cap && w < W - 1) { ++w; used = 0; }
+  bool w_used = false;
+  int64_t cum = 0;
+  auto advance = [&]() {
+    while (w < W - 1 && cum >= bound(w)) { ++w; w_used = false; }
   };
   for (int b = 0; b < batch; ++b) {
     if (tiles[b] == 0) {
       p->segs.push_back(Segment{b, 0, 0, -1});
       p->seg_worker.push_back(w);
-      used += kSegOverheadTiles;
-      close_if_full();
+      w_used = true;
+      cum += kSegOverheadTiles;
+      advance();
       continue;
     }
     int64_t t = 0;
     while (t < tiles[b]) {
       const int64_t left = tiles[b] - t;
-      const int64_t room = cap - used - kSegOverheadTiles;
-      if (w < W - 1 && used > 0 && room < std::min<int64_t>(left, kMinSplitTiles)) {
-        ++w; used = 0;
-        continue;
+      const int64_t room = bound(w) - cum - kSegOverheadTiles;
+      int64_t n;
+      if (w == W - 1 || left <= room) {
+        n = left;
+      } else if (room < kMinSplitTiles) {
+        if (w_used) { ++w; w_used = false; continue; }
+        n = std::min<int64_t>(left, kMinSplitTiles);
+      } else {
+        n = room;
+        if (left - n < kMinSplitTiles) n = (left - kMinSplitTiles >= kMinSplitTiles) ? left - kMinSplitTiles : left;
       }
-      int64_t n = (w == W - 1) ? left : std::min(left, std::max<int64_t>(room, kMinSplitTiles));
-      if (left - n < kMinSplitTiles) n = left;
       p->segs.push_back(Segment{b, (int32_t)t, (int32_t)(t + n), -1});
       p->seg_worker.push_back(w);
-      used += kSegOverheadTiles + n;
+      w_used = true;
+      cum += n + kSegOverheadTiles;
       t += n;
-      close_if_full();
+      advance();
     }
+  }
+  nsegs = (int64_t)p->segs.size();
   }
 
   // split counts and partial slots

@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(128) simt_decode_kernel(const __grid_constant_
     if (sg.slot < 0)
       reinterpret_cast<__nv_bfloat16*>(a.out)[orow * kLatent + c] = __float2bfloat16_rn(acc);
     else
-      a.part_o[((size_t)sg.slot * a.rows + m) * kLatent + c] = acc;
+      a.part_o[(((size_t)sg.slot * (kLatent / 4) + c / 4) * a.rows + m) * 4 + (c & 3)] = acc;  // chunk-major
   }
   if (threadIdx.x == 0) {
     if (sg.slot < 0) a.lse[orow] = lse;

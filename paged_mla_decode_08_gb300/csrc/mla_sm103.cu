@@ -16,15 +16,17 @@
 // operand of S, MN-major as the B operand of P.V.  The 128 query rows
 // (heads x q_len, zero-padded) are the M dimension of every MMA.
 //
-// TMEM (512 columns): O [0,256), S double buffer [256,320) / [320,384) (P is
-// written over the S it came from, as bf16 pairs), Q latent half [384,512).
-// Shared memory: 4-stage cache-tile ring (36 KB per stage), the rope half of
-// Q (8 KB), two 32 KB score-exchange buffers written by the peer CTA.
+// TMEM (512 columns): O [0,256), S double buffer [256,320) / [320,384), Q
+// latent half [384,512).  Shared memory: 4-stage cache-tile ring (36 KB per
+// stage), the rope half of Q (8 KB), the P tile (16 KB, the A operand of
+// P.V), a 3-slot ring of half-tile score-exchange buffers (16 KB each)
+// written by the peer CTA.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and
+// Warp roles (512 threads): warp 0 TMA producer, warp 1 TMEM allocator and
 // MMA issuer, warps 4-11 softmax / correction / epilogue (two warps per query
 // row block = TMEM lane quadrant, each owning half of a tile's keys and half
-// of the output columns), warps 2-3 spare.  Every wait is bounded: on timeout the kernel
+// of the output columns), warps 12-15 score exchange with the peer CTA,
+// warps 2-3 spare.  Every wait is bounded: on timeout the kernel
 // records an error code in device memory, stops every role, waits for its
 // own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -44,7 +46,7 @@ namespace sm103 {
 
 using namespace mla::ptx;
 
-constexpr int kThreads = 384;  // warps 0-3: producer, MMA, 2 spare; 4-11: softmax
+constexpr int kThreads = 512;  // warps 0-3: producer, MMA, 2 spare; 4-11: softmax; 12-15: exchange
 constexpr int kStages = 4;
 constexpr int kLatBox = 64 * 128;           // 64 tokens x 64 bf16 columns, 128B swizzle
 constexpr int kRopeBox = 64 * 64;           // 64 tokens x 32 bf16 columns, 64B swizzle
@@ -52,18 +54,25 @@ constexpr int kStageBytes = 4 * kLatBox + kRopeBox;  // 36864
 constexpr int kStageTx = kStageBytes;       // bytes TMA delivers per tile
 constexpr int OFF_KV = 0;
 constexpr int OFF_QROPE = kStages * kStageBytes;       // 128 rows x 64 B
-constexpr int OFF_XCHG = OFF_QROPE + 128 * 64;         // 2 x (128 rows x 256 B)
-constexpr int kXchgBytes = 128 * 64 * 4;
-constexpr int OFF_RED = OFF_XCHG + 2 * kXchgBytes;     // row max / row sum exchange, 4 KB
-constexpr int OFF_SINK = OFF_RED + 4 * 2 * 128 * 4;    // 2 x 256 words the peer's "read done" notes land in
-constexpr int kNoteBytes = 256 * 4;
-constexpr int OFF_BAR = OFF_SINK + 2 * kNoteBytes;
+constexpr int OFF_P = OFF_QROPE + 128 * 64;            // P (128 rows x 64 keys bf16, 128B swizzle)
+constexpr int kPBytes = 128 * 128;
+// Score exchange: a ring of 3 slots, each holding the peer's partial scores
+// of one half tile (32 keys) for 128 rows, [16-byte chunk][row] fp32.
+constexpr int kSlots = 3;
+constexpr int OFF_XCHG = OFF_P + kPBytes;
+constexpr int kSlotBytes = 128 * 32 * 4;
+constexpr int OFF_RED = OFF_XCHG + kSlots * kSlotBytes;  // row max / row sum exchange, 4 KB
+constexpr int OFF_SINK = OFF_RED + 4 * 2 * 128 * 4;      // per slot 128 words: the peer's "read done" notes
+constexpr int kNoteBytes = 128 * 4;
+constexpr int OFF_BAR = OFF_SINK + kSlots * kNoteBytes;
 enum Bar : int {
   B_KV_FULL = 0, B_KV_EMPTY = B_KV_FULL + kStages, B_S_FULL = B_KV_EMPTY + kStages, B_P_FULL = B_S_FULL + 2,
-  B_PV_DONE = B_P_FULL + 2, B_Q_READY, B_X_FULL, B_X_EMPTY = B_X_FULL + 2, B_TAIL = B_X_EMPTY + 2, B_FINAL,
+  B_PV_DONE, B_Q_READY, B_X_FULL, B_X_EMPTY = B_X_FULL + kSlots, B_TAIL = B_X_EMPTY + kSlots, B_FINAL,
   B_PAIR_MAX,                 // [quad][tile parity]: the two warps of a quadrant swap row maxima
   B_PAIR_L = B_PAIR_MAX + 8,  // [quad]: ... and row sums at a segment's end
-  B_COUNT = B_PAIR_L + 4
+  B_S_LOADED = B_PAIR_L + 4,  // [tile parity]: exchange warps hold S in registers
+  B_S_FREE = B_S_LOADED + 2,  // [tile parity]: softmax warps too; the S buffer may take the next S
+  B_COUNT = B_S_FREE + 2
 };
 constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
@@ -141,6 +150,15 @@ __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeA
     const int L = request_len(a, sg.req);
     const int nt = segment_tiles(sg, L);
     const int32_t* bt = a.block_table + (size_t)sg.req * a.bt_stride;
+    if (nt > 0 && lane == 0) {
+      // the exchange warps load this request's query when the segment
+      // starts: pull it into L2 now, a few tiles ahead (the M rows are
+      // contiguous; 16-byte multiples)
+      prefetch_l2_bulk(reinterpret_cast<const __nv_bfloat16*>(a.q_nope) + (size_t)sg.req * a.rows * kLatent,
+                       (uint32_t)a.rows * kLatent * 2);
+      prefetch_l2_bulk(reinterpret_cast<const __nv_bfloat16*>(a.q_pe) + (size_t)sg.req * a.rows * kRope,
+                       (uint32_t)a.rows * kRope * 2);
+    }
     for (int jj = 0; jj < nt; ++jj, ++j) {
       const int stage = j % kStages;
       if (j >= kStages && !wait_bar_warp<false>(c, c.bar(B_KV_EMPTY + stage), ((j / kStages) - 1) & 1, 0x101)) {
@@ -203,53 +221,86 @@ __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeA
 
 template <int CAP>
 __device__ void mma_issuer(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, uint32_t tmem, int worker) {
-  int j = 0, segs_run = 0;
-  bool ok = true;
-  auto issue_pv = [&](int jp, bool first) -> bool {
-    const int pb = jp & 1;
-    if (!wait_bar<false>(c, c.bar(B_P_FULL + pb), (jp >> 1) & 1, 0x203)) return false;
-    tc_fence_after();
-    const uint32_t stage_addr = c.sbase + OFF_KV + (jp % kStages) * kStageBytes;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      // B = V (tokens x 256 latent), MN-major 128B swizzle: 64-column atoms
-      // 8 KB apart (LBO), 8-token row groups 1 KB apart (SBO)
-      const uint64_t bdesc = smem_desc(stage_addr + kk * 16 * 128, kLatBox, 1024, kSwizzle128B);
-      mma_ts(tmem + TM_O, tmem + TM_S + 64 * pb + 8 * kk, bdesc, kIdescPV, (first && kk == 0) ? 0u : 1u);
-    }
-    mma_commit(c.bar(B_PV_DONE));
-    mma_commit(c.bar(B_KV_EMPTY + (jp % kStages)));
-    return true;
+  // Two cursors walk this worker's tile sequence: S products run ahead as
+  // soon as a cache tile has landed and the S buffer they write was read by
+  // the softmax warps; P.V products follow as P tiles appear.  Whichever is
+  // ready is issued, so S of tile j+2 never waits for P.V of tile j.
+  const int seg_end = sched.worker_seg[worker + 1];
+  auto first_live = [&](int s) {
+    while (s < seg_end && segment_tiles(sched.seg[s], request_len(a, sched.seg[s].req)) == 0) ++s;
+    return s;
   };
-  for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
-    const Segment sg = sched.seg[s];
-    const int nt = segment_tiles(sg, request_len(a, sg.req));
-    if (nt == 0) continue;
-    if (!wait_bar<false>(c, c.bar(B_Q_READY), segs_run & 1, 0x201)) { ok = false; break; }
-    ++segs_run;
-    tc_fence_after();
-    for (int jj = 0; jj < nt; ++jj, ++j) {
-      const int stage = j % kStages;
-      if (!wait_bar<false>(c, c.bar(B_KV_FULL + stage), (j / kStages) & 1, 0x202)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t stage_addr = c.sbase + OFF_KV + stage * kStageBytes;
-      const uint32_t d = tmem + TM_S + 64 * (j & 1);
+  int s_seg = first_live(sched.worker_seg[worker]), s_jj = 0, s_j = 0, q_used = 0;
+  int p_seg = s_seg, p_jj = 0, p_j = 0;
+  int s_nt = s_seg < seg_end ? segment_tiles(sched.seg[s_seg], request_len(a, sched.seg[s_seg].req)) : 0;
+  int p_nt = s_nt;
+  long long t_last = clock64();
+  while (p_seg < seg_end) {
+    bool progressed = false;
+    if (s_seg < seg_end) {
+      const int stage = s_j % kStages;
+      bool ready = (s_jj > 0 || mbar_test_wait(c.bar(B_Q_READY), q_used & 1)) &&
+                   mbar_test_wait(c.bar(B_KV_FULL + stage), (s_j / kStages) & 1) &&
+                   (s_j < 2 || mbar_test_wait(c.bar(B_S_FREE + (s_j & 1)), ((s_j >> 1) - 1) & 1));
+      if (ready) {
+        if (s_jj == 0) ++q_used;
+        tc_fence_after();
+        const uint32_t stage_addr = c.sbase + OFF_KV + stage * kStageBytes;
+        const uint32_t d = tmem + TM_S + 64 * (s_j & 1);
 #pragma unroll
-      for (int kk = 0; kk < 16; ++kk) {
-        // B = cache latent half (64 tokens x 256), K-major 128B swizzle
-        const uint64_t bdesc = smem_desc(stage_addr + (kk >> 2) * kLatBox + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-        mma_ts(d, tmem + TM_Q + 8 * kk, bdesc, kIdescS, kk > 0 ? 1u : 0u);
-      }
+        for (int kk = 0; kk < 16; ++kk) {
+          // B = cache latent half (64 tokens x 256), K-major 128B swizzle
+          const uint64_t bdesc = smem_desc(stage_addr + (kk >> 2) * kLatBox + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          mma_ts(d, tmem + TM_Q + 8 * kk, bdesc, kIdescS, kk > 0 ? 1u : 0u);
+        }
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const uint64_t adesc = smem_desc(c.sbase + OFF_QROPE + kk * 32, 16, 512, kSwizzle64B);
-        const uint64_t bdesc = smem_desc(stage_addr + 4 * kLatBox + kk * 32, 16, 512, kSwizzle64B);
-        mma_ss(d, adesc, bdesc, kIdescS, 1u);
+        for (int kk = 0; kk < 2; ++kk) {
+          const uint64_t adesc = smem_desc(c.sbase + OFF_QROPE + kk * 32, 16, 512, kSwizzle64B);
+          const uint64_t bdesc = smem_desc(stage_addr + 4 * kLatBox + kk * 32, 16, 512, kSwizzle64B);
+          mma_ss(d, adesc, bdesc, kIdescS, 1u);
+        }
+        mma_commit(c.bar(B_S_FULL + (s_j & 1)));
+        ++s_j;
+        if (++s_jj == s_nt) {
+          s_jj = 0;
+          s_seg = first_live(s_seg + 1);
+          s_nt = s_seg < seg_end ? segment_tiles(sched.seg[s_seg], request_len(a, sched.seg[s_seg].req)) : 0;
+        }
+        progressed = true;
       }
-      mma_commit(c.bar(B_S_FULL + (j & 1)));
-      if (jj > 0 && !issue_pv(j - 1, jj == 1)) { ok = false; break; }
     }
-    if (ok && !issue_pv(j - 1, nt == 1)) ok = false;
+    if (p_j < s_j && mbar_test_wait(c.bar(B_P_FULL), p_j & 1)) {
+      tc_fence_after();
+      const uint32_t stage_addr = c.sbase + OFF_KV + (p_j % kStages) * kStageBytes;
+      const uint32_t p_addr = c.sbase + OFF_P;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        // A = P (128 rows x 64 keys) K-major 128B swizzle; B = V (keys x 256
+        // latent) MN-major 128B swizzle: 64-column atoms 8 KB apart (LBO),
+        // 8-key row groups 1 KB apart (SBO)
+        const uint64_t adesc = smem_desc(p_addr + kk * 32, 16, 1024, kSwizzle128B);
+        const uint64_t bdesc = smem_desc(stage_addr + kk * 16 * 128, kLatBox, 1024, kSwizzle128B);
+        mma_ss(tmem + TM_O, adesc, bdesc, kIdescPV, (p_jj == 0 && kk == 0) ? 0u : 1u);
+      }
+      mma_commit(c.bar(B_PV_DONE));
+      mma_commit(c.bar(B_KV_EMPTY + (p_j % kStages)));
+      ++p_j;
+      if (++p_jj == p_nt) {
+        p_jj = 0;
+        p_seg = first_live(p_seg + 1);
+        p_nt = p_seg < seg_end ? segment_tiles(sched.seg[p_seg], request_len(a, sched.seg[p_seg].req)) : 0;
+      }
+      progressed = true;
+    }
+    if (progressed) {
+      t_last = clock64();
+    } else if (*c.abort_flag) {
+      break;
+    } else if (clock64() - t_last > kTimeoutCycles) {
+      *c.abort_flag = 1;
+      atomicCAS(&g_kernel_error, 0, 0x204);
+      break;
+    }
   }
   // all issued tensor-core work must finish before TMEM is released
   mma_commit(c.bar(B_FINAL));
@@ -267,6 +318,100 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& rlo, fl
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// ------------------------------------------------------------------ exchange
+
+// Warps 12-15 (one per TMEM lane quadrant, thread = query row): as soon as a
+// tile's partial scores land in TMEM, copy them to registers and stream them
+// into the peer CTA's receive buffer with st.async, which completes bytes on
+// the peer's x_full barrier.  Decoupled from the softmax warps so that the
+// ~0.5 us it takes to issue 32 KB of remote stores never blocks them.
+template <int CAP>
+__device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, uint32_t tmem, int worker,
+                          int rank) {
+  const int quad = (threadIdx.x >> 5) & 3;
+  const int row = quad * 32 + (threadIdx.x & 31);
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t peer = rank ^ 1;
+  const uint32_t xchg_peer = mapa(c.sbase + OFF_XCHG, peer) + row * 16;
+  const uint32_t x_full_peer = mapa(c.bar(B_X_FULL), peer);  // slot k's barrier at + 8k
+  const int M = a.rows;
+  const bool valid_row = row < M;  // padding rows (M < 128) exchange nothing
+  int j = 0;
+  bool ok = true;
+  for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
+    const Segment sg = sched.seg[s];
+    const int nt = segment_tiles(sg, request_len(a, sg.req));
+    if (nt == 0) continue;
+    // ---- this segment's query: latent half -> TMEM columns [384, 512), rope
+    // half -> shared memory (64B swizzle).  The previous segment's S MMAs all
+    // completed (this warp waited for each), so the old Q is dead; the load
+    // overlaps the softmax warps' last tile and epilogue.
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q_nope) +
+                                                        ((size_t)sg.req * M + row) * kLatent + 256 * rank);
+      const uint4* srp = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q_pe) +
+                                                        ((size_t)sg.req * M + row) * kRope + 32 * rank);
+      uint4 rp[4];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) rp[ch] = valid_row ? __ldg(srp + ch) : make_uint4(0, 0, 0, 0);
+      // two rounds of 16 independent 16-byte loads (one latency each)
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        uint4 q[16];
+#pragma unroll
+        for (int v = 0; v < 16; ++v) q[v] = valid_row ? __ldg(src + hh * 16 + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int ck = 0; ck < 2; ++ck) {
+          uint32_t r[32];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            r[4 * v + 0] = q[8 * ck + v].x; r[4 * v + 1] = q[8 * ck + v].y;
+            r[4 * v + 2] = q[8 * ck + v].z; r[4 * v + 3] = q[8 * ck + v].w;
+          }
+          tmem_st32(tmem + lane_off + TM_Q + 64 * hh + 32 * ck, r);
+        }
+      }
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+        st_shared_v4(c.sbase + OFF_QROPE + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4), rp[ch]);
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(c.bar(B_Q_READY));
+    }
+    for (int jj = 0; jj < nt; ++jj, ++j) {
+      const int sb = j & 1, u = j >> 1;
+      if (!wait_bar_warp<false>(c, c.bar(B_S_FULL + sb), u & 1, 0x401)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t s0[32], s1[32];
+      tmem_ld32(tmem + lane_off + TM_S + 64 * sb, s0);
+      tmem_ld32(tmem + lane_off + TM_S + 64 * sb + 32, s1);
+      tmem_ld_wait(s0);
+      tmem_ld_wait(s1);
+      tc_fence_before();
+      mbar_arrive(c.bar(B_S_LOADED + sb));
+      // the two 32-key halves go to ring slots (2j) % 3 and (2j + 1) % 3;
+      // a slot's previous half must have been read by the peer
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int g = 2 * j + h, k = g % kSlots, ug = g / kSlots;
+        if (ug > 0 && !wait_bar_warp<true>(c, c.bar(B_X_EMPTY + k), (ug - 1) & 1, 0x402)) { ok = false; break; }
+        const uint32_t dst = xchg_peer + k * kSlotBytes;
+        const uint32_t mb = x_full_peer + 8 * k;
+        const uint32_t* sv = h ? s1 : s0;
+        if (valid_row) {
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            st_async_v4(dst + ch * 2048, sv[4 * ch], sv[4 * ch + 1], sv[4 * ch + 2], sv[4 * ch + 3], mb);
+        }
+        // arm the "peer has read it" phase of this slot: one 4-byte note per live row
+        if (threadIdx.x == 384) mbar_arrive_expect_tx(c.bar(B_X_EMPTY + k), 4 * M);
+      }
+      if (!ok) break;
+    }
+  }
+}
+
 template <int CAP>
 __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, uint32_t tmem,
                                  int worker, int rank) {
@@ -282,42 +427,17 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
   const int M = a.rows;
   const bool valid_row = row < M;
   const int qi = valid_row ? row / a.num_heads : 0;  // query position of this row
-  // Exchange buffers, [16-byte chunk][row] so a warp's stores are contiguous.
-  // This thread's 8 chunks start at chunk 8*half.
-  const uint32_t my_off = static_cast<uint32_t>((half * 8 * 128 + row) * 16);
-  const uint32_t xchg_local = c.sbase + OFF_XCHG + my_off;
-  const uint32_t xchg_peer = mapa(c.sbase + OFF_XCHG, peer) + my_off;
-  const uint32_t x_full_peer0 = mapa(c.bar(B_X_FULL), peer), x_full_peer1 = mapa(c.bar(B_X_FULL + 1), peer);
-  const uint32_t x_empty_peer0 = mapa(c.bar(B_X_EMPTY), peer), x_empty_peer1 = mapa(c.bar(B_X_EMPTY + 1), peer);
-  const uint32_t sink_peer = mapa(c.sbase + OFF_SINK, peer) + (threadIdx.x - 128) * 4;
+  // Exchange ring slots hold [16-byte chunk][row] so a warp's stores are
+  // contiguous; half tile g = 2j + half of this thread sits in slot g % 3.
+  const uint32_t xchg_local = c.sbase + OFF_XCHG + row * 16;
+  const uint32_t x_empty_peer = mapa(c.bar(B_X_EMPTY), peer);  // slot k's barrier at + 8k
+  const uint32_t sink_peer = mapa(c.sbase + OFF_SINK, peer) + row * 4;
+  const uint32_t rearm_thread = 128 + 128 * half;  // re-arms this half's slots
   float* red_max = reinterpret_cast<float*>(c.smem + OFF_RED);      // [2 tiles][2 halves][128]
   float* red_l = red_max + 2 * 2 * 128;                              // [2 segments][2 halves][128]
   const float cs = a.score_scale_log2;  // raw score -> base-2 logit
   int j = 0, nseg = 0;
   bool ok = true;
-
-  // S partial of tile jn (this thread's 32 columns) from TMEM
-  auto load_s = [&](int jn, uint32_t(&sv)[32]) -> bool {
-    const int sb = jn & 1;
-    if (!wait_bar_warp<false>(c, c.bar(B_S_FULL + sb), (jn >> 1) & 1, 0x301)) return false;
-    tc_fence_after();
-    tmem_ld32(tmem + lane_off + TM_S + 64 * sb + 32 * half, sv);
-    tmem_ld_wait(sv);
-    return true;
-  };
-  // ... and into the peer CTA's exchange buffer
-  auto send = [&](int jn, const uint32_t(&sv)[32]) -> bool {
-    const int sb = jn & 1, u = jn >> 1;
-    if (u > 0 && !wait_bar_warp<true>(c, c.bar(B_X_EMPTY + sb), (u - 1) & 1, 0x302)) return false;
-    const uint32_t dst = xchg_peer + sb * kXchgBytes;
-    const uint32_t mb = sb ? x_full_peer1 : x_full_peer0;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-      st_async_v4(dst + ch * 2048, sv[4 * ch], sv[4 * ch + 1], sv[4 * ch + 2], sv[4 * ch + 3], mb);
-    // arm the "peer has read it" phase of this buffer: 256 four-byte notes
-    if (threadIdx.x == 128) mbar_arrive_expect_tx(c.bar(B_X_EMPTY + sb), kNoteBytes);
-    return true;
-  };
 
   for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
     const Segment sg = sched.seg[s];
@@ -328,49 +448,28 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
     float m_ref = -CUDART_INF_F, l = 0.f;
 
     if (nt > 0) {
-      // ---- Q: latent half -> TMEM columns [384, 512) (this thread: 128 of
-      // the 256 elements), rope half -> shared memory (64B swizzle)
-      {
-        uint32_t r[32];
-        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q_nope) +
-                                                          ((size_t)b * M + row) * kLatent + 256 * rank + 128 * half);
-#pragma unroll
-        for (int ck = 0; ck < 2; ++ck) {
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const uint4 q4 = valid_row ? __ldg(src + ck * 8 + v) : make_uint4(0, 0, 0, 0);
-            r[4 * v + 0] = q4.x; r[4 * v + 1] = q4.y; r[4 * v + 2] = q4.z; r[4 * v + 3] = q4.w;
-          }
-          tmem_st32(tmem + lane_off + TM_Q + 64 * half + 32 * ck, r);
-        }
-        const uint4* srp = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q_pe) +
-                                                          ((size_t)b * M + row) * kRope + 32 * rank + 16 * half);
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int ch = 2 * half + i;
-          const uint4 q4 = valid_row ? __ldg(srp + i) : make_uint4(0, 0, 0, 0);
-          st_shared_v4(c.sbase + OFF_QROPE + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4), q4);
-        }
-        tmem_st_wait();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(c.bar(B_Q_READY));
-      }
 
-      uint32_t cur[32];  // own partial scores of the tile being finished
-      if (!load_s(j, cur) || !send(j, cur)) { ok = false; break; }
       for (int jj = 0; jj < nt; ++jj, ++j) {
         const int sb = j & 1;
-        // ---- the next tile's exchange first, so its DSMEM transit overlaps this tile
-        uint32_t nxt[32];
-        if (jj + 1 < nt && (!load_s(j + 1, nxt) || !send(j + 1, nxt))) { ok = false; break; }
+        // ---- own partial scores: the exchange warps have read S out of
+        // TMEM (so P may overwrite it later); this thread's 32 columns
+        if (!wait_bar_warp<false>(c, c.bar(B_S_LOADED + sb), (j >> 1) & 1, 0x301)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t cur[32];
+        tmem_ld32(tmem + lane_off + TM_S + 64 * sb + 32 * half, cur);
+        tmem_ld_wait(cur);
+        tc_fence_before();
+        mbar_arrive(c.bar(B_S_FREE + sb));  // the MMA may overwrite this S buffer
         // ---- full scores: own partial + the peer's (its st.async bytes
-        // complete the transaction count this CTA expects per tile)
-        if (threadIdx.x == 128) mbar_arrive_expect_tx(c.bar(B_X_FULL + sb), kXchgBytes);
-        if (!wait_bar_warp<true>(c, c.bar(B_X_FULL + sb), (j >> 1) & 1, 0x303)) { ok = false; break; }
+        // complete the transaction count armed for this phase).  Re-arming
+        // the next phase right away is safe: the peer cannot send into this
+        // slot again before all "read" notes of this phase reached it.
+        const int g = 2 * j + half, slot = g % kSlots, ug = g / kSlots;
+        if (!wait_bar_warp<true>(c, c.bar(B_X_FULL + slot), ug & 1, 0x303)) { ok = false; break; }
+        if (threadIdx.x == rearm_thread) mbar_arrive_expect_tx(c.bar(B_X_FULL + slot), 128 * M);
         float x[32];
         {
-          const uint32_t srcx = xchg_local + sb * kXchgBytes;
+          const uint32_t srcx = xchg_local + slot * kSlotBytes;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             const uint4 v = ld_shared_v4(srcx + ch * 2048);
@@ -400,7 +499,7 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
         }
         // tell the peer its buffer is free: a 4-byte st.async whose value (the
         // row max) depends on every word read from the buffer
-        st_async_b32(sink_peer + sb * kNoteBytes, __float_as_uint(mt), sb ? x_empty_peer1 : x_empty_peer0);
+        if (valid_row) st_async_b32(sink_peer + slot * kNoteBytes, __float_as_uint(mt), x_empty_peer + 8 * slot);
         red_max[(sb * 2 + half) * 128 + row] = mt;
         mbar_arrive(c.bar(B_PAIR_MAX + 2 * quad + sb));
         if (!wait_bar_warp<false>(c, c.bar(B_PAIR_MAX + 2 * quad + sb), (j >> 1) & 1, 0x306)) { ok = false; break; }
@@ -433,7 +532,8 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
           m_ref = m_new;
         }
         const float nm = m_ref == -CUDART_INF_F ? 0.f : -m_ref;  // all-masked rows: 2^-inf = 0
-        // ---- P (bf16 pairs) over the S columns it came from
+        // ---- P (bf16 pairs) to shared memory, K-major 128B swizzle: this
+        // thread's 32 keys are 16-byte chunks 4*half..4*half+3 of its row
         uint32_t pk[16];
         float lsum = 0.f;
 #pragma unroll
@@ -445,12 +545,15 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
           lsum += p0 + p1;  // l from the unrounded probabilities: exact lse
         }
         l += lsum;
-        tmem_st16(tmem + lane_off + TM_S + 64 * sb + 16 * half, pk);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(c.bar(B_P_FULL + sb));
+        {
+          const uint32_t prow = c.sbase + OFF_P + row * 128;  // free: P.V of the previous tile is done
 #pragma unroll
-        for (int k = 0; k < 32; ++k) cur[k] = nxt[k];
+          for (int i = 0; i < 4; ++i)
+            st_shared_v4(prow + (((4 * half + i) ^ (row & 7)) << 4),
+                         make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(c.bar(B_P_FULL));
       }
       if (!ok) break;
       if (!wait_bar_warp<false>(c, c.bar(B_PV_DONE), (j - 1) & 1, 0x305)) { ok = false; break; }
@@ -498,11 +601,13 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
             dst[v] = w;
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)sg.slot * M + row) * kLatent + col);
+          // partials are chunk-major, [slot][16-byte chunk][row]: a warp's
+          // 32 rows store 512 contiguous bytes
+          float4* dst = reinterpret_cast<float4*>(a.part_o) + ((size_t)sg.slot * (kLatent / 4) + col / 4) * M + row;
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(o[4 * v + 0]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                 __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+            dst[(size_t)v * M] = make_float4(__uint_as_float(o[4 * v + 0]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                             __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
         }
       }
       if (rank == 0 && half == 0 && valid_row) {
@@ -538,18 +643,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(c.bar(B_KV_FULL + s), 1);
       mbar_init(c.bar(B_KV_EMPTY + s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(c.bar(B_S_FULL + i), 1);
-      mbar_init(c.bar(B_P_FULL + i), 256);
-      mbar_init(c.bar(B_X_FULL + i), 1);  // own expect_tx arrival + the peer's st.async bytes
-      mbar_init(c.bar(B_X_EMPTY + i), 1);  // own expect_tx arrival + the peer's 4-byte notes
+    for (int i = 0; i < 2; ++i) mbar_init(c.bar(B_S_FULL + i), 1);
+    mbar_init(c.bar(B_P_FULL), 256);
+    for (int k = 0; k < kSlots; ++k) {
+      mbar_init(c.bar(B_X_FULL + k), 1);   // own expect_tx arrival + the peer's st.async bytes
+      mbar_init(c.bar(B_X_EMPTY + k), 1);  // own expect_tx arrival + the peer's 4-byte notes
     }
     mbar_init(c.bar(B_PV_DONE), 1);
-    mbar_init(c.bar(B_Q_READY), 256);
+    mbar_init(c.bar(B_Q_READY), 128);
     mbar_init(c.bar(B_TAIL), 1);
     mbar_init(c.bar(B_FINAL), 1);
     for (int i = 0; i < 8; ++i) mbar_init(c.bar(B_PAIR_MAX + i), 64);
+    // receive buffers are armed one phase ahead: phase 0 now, phase u+1 as
+    // soon as phase u completed (so the peer's bytes never precede the arm)
+    for (int k = 0; k < kSlots; ++k) mbar_arrive_expect_tx(c.bar(B_X_FULL + k), 128 * a.rows);
     for (int i = 0; i < 4; ++i) mbar_init(c.bar(B_PAIR_L + i), 64);
+    for (int i = 0; i < 2; ++i) mbar_init(c.bar(B_S_LOADED + i), 128);
+    for (int i = 0; i < 2; ++i) mbar_init(c.bar(B_S_FREE + i), 256);
     fence_mbar_init();
     prefetch_tensormap(&tm_lat);
     prefetch_tensormap(&tm_rope);
@@ -570,6 +680,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       if ((threadIdx.x & 31) == 0) mma_issuer<CAP>(c, sched, a, tmem, worker);
       __syncwarp();
+    } else if (warp >= 12) {
+      exchanger<CAP>(c, sched, a, tmem, worker, rank);
     } else if (warp >= 4) {
       softmax_epilogue<CAP>(c, sched, a, tmem, worker, rank);
     }
