@@ -14,7 +14,6 @@
 #include "mla_internal.h"
 
 namespace mla {
-cudaError_t launch_simt(const mla_plan& p, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_sm103(const mla_plan& p, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t sm103_read_error(int* code, bool reset);
 cudaError_t launch_combine(const std::vector<CombineJob>& jobs, const DecodeArgs& a,
@@ -109,18 +108,8 @@ int prepare(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_
   return MLA_OK;
 }
 
-int use_simt() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("MLA_DEV_SIMT");
-    v = (e && e[0] == '1') ? 1 : 0;
-  }
-  return v;
-}
-
 int launch_main(const mla_plan* plan, const Prepared& pr, cudaStream_t stream) {
-  const bool simt = use_simt() || pr.args.kv_dtype == MLA_KV_E4M3;
-  cudaError_t e = simt ? mla::launch_simt(*plan, pr.args, stream) : mla::launch_sm103(*plan, pr.args, stream);
+  cudaError_t e = mla::launch_sm103(*plan, pr.args, stream);
   if (e == cudaErrorNotSupported)
     return fail(MLA_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled unavailable or rejected the cache layout");
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("main kernel launch: ") + cudaGetErrorString(e));

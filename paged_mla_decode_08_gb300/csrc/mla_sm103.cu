@@ -26,9 +26,18 @@
 // MMA issuer, warps 4-11 softmax / correction / epilogue (two warps per query
 // row block = TMEM lane quadrant, each owning half of a tile's keys and half
 // of the output columns), warps 12-15 score exchange with the peer CTA,
-// warps 2-3 spare.  Every wait is bounded: on timeout the kernel
-// records an error code in device memory, stops every role, waits for its
-// own copies and MMAs, frees TMEM and returns.
+// warps 2-3 e4m3 -> fp16 converters (float8 cache only).  Every wait is
+// bounded: on timeout the kernel records an error code in device memory,
+// stops every role, waits for its own copies and MMAs, frees TMEM and
+// returns.
+//
+// Float8 (e4m3) cache.  The same kernel, instantiated with F8 = true: TMA
+// brings raw e4m3 tiles (half the bytes) into a 4-stage fp8 ring, the two
+// converter warps expand each tile into an fp16 operand stage laid out like
+// a bf16 stage (cvt.rn.f16x2.e4m3x2 is exact), and the MMAs run on fp16
+// operands (the query is converted to fp16 once per segment, P is packed
+// to fp16).  The per-tensor scale k_scale multiplies the scores and the
+// output (it is folded into the score scale and the epilogue scale).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -46,13 +55,23 @@ namespace sm103 {
 
 using namespace mla::ptx;
 
-constexpr int kThreads = 512;  // warps 0-3: producer, MMA, 2 spare; 4-11: softmax; 12-15: exchange
-constexpr int kStages = 4;
+constexpr int kThreads = 512;  // warps 0-3: producer, MMA, 2 converter (e4m3); 4-11: softmax; 12-15: exchange
+constexpr int kStages = 4;  // bf16 cache: operand stages; e4m3 cache: fp8 staging stages
 constexpr int kLatBox = 64 * 128;           // 64 tokens x 64 bf16 columns, 128B swizzle
 constexpr int kRopeBox = 64 * 64;           // 64 tokens x 32 bf16 columns, 64B swizzle
 constexpr int kStageBytes = 4 * kLatBox + kRopeBox;  // 36864
 constexpr int kStageTx = kStageBytes;       // bytes TMA delivers per tile
 constexpr int OFF_KV = 0;
+// e4m3 cache: the first 144 KB hold 2 fp16 operand stages (same layout as a
+// bf16 stage) followed by 4 fp8 staging stages, each 64 keys x (256 latent +
+// 32 rope) bytes, unswizzled.
+constexpr int kF8OpStages = 2;
+constexpr int kF8StageBytes = 64 * 288;
+constexpr int kF8RopeOff = 64 * 256;
+constexpr int OFF_F8 = kF8OpStages * kStageBytes;
+static_assert(OFF_F8 + kStages * kF8StageBytes == kStages * kStageBytes, "fp8 ring fits the operand ring");
+template <bool F8>
+__host__ __device__ constexpr int op_stages() { return F8 ? kF8OpStages : kStages; }
 constexpr int OFF_QROPE = kStages * kStageBytes;       // 128 rows x 64 B
 constexpr int OFF_P = OFF_QROPE + 128 * 64;            // P (128 rows x 64 keys bf16, 128B swizzle)
 constexpr int kPBytes = 128 * 128;
@@ -72,7 +91,9 @@ enum Bar : int {
   B_PAIR_L = B_PAIR_MAX + 8,  // [quad]: ... and row sums at a segment's end
   B_S_LOADED = B_PAIR_L + 4,  // [tile parity]: exchange warps hold S in registers
   B_S_FREE = B_S_LOADED + 2,  // [tile parity]: softmax warps too; the S buffer may take the next S
-  B_COUNT = B_S_FREE + 2
+  B_F8_FULL = B_S_FREE + 2,   // [fp8 stage]: TMA delivered the raw e4m3 tile
+  B_F8_EMPTY = B_F8_FULL + kStages,  // [fp8 stage]: converted, may be refilled
+  B_COUNT = B_F8_EMPTY + kStages
 };
 constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
@@ -80,8 +101,11 @@ constexpr int kSmemUsed = OFF_ABORT + 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 
 constexpr uint32_t TM_O = 0, TM_S = 256, TM_Q = 384, kTmemCols = 512;
-constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, 0, 0);
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, 0, 1);
+// bf16 cache: bf16 operands; e4m3 cache: fp16 operands (e4m3 -> fp16 is exact)
+template <bool F8>
+__host__ __device__ constexpr uint32_t idesc_s() { return idesc_f32acc(128, 64, 0, 0, F8 ? 0u : 1u); }
+template <bool F8>
+__host__ __device__ constexpr uint32_t idesc_pv() { return idesc_f32acc(128, 256, 0, 1, F8 ? 0u : 1u); }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
 constexpr long long kTimeoutCycles = 2000000000LL;
 
@@ -137,7 +161,7 @@ __device__ __forceinline__ int segment_tiles(const Segment& sg, int L) {
 
 // ------------------------------------------------------------------ producer
 
-template <int CAP>
+template <int CAP, bool F8>
 __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, const CUtensorMap* tm_lat,
                          const CUtensorMap* tm_rope, int worker, int rank) {
   const int lane = threadIdx.x & 31;
@@ -161,6 +185,32 @@ __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeA
     }
     for (int jj = 0; jj < nt; ++jj, ++j) {
       const int stage = j % kStages;
+      if (F8) {
+        // raw e4m3 tile into the fp8 ring; the converter warps expand it
+        if (j >= kStages && !wait_bar_warp<false>(c, c.bar(B_F8_EMPTY + stage), ((j / kStages) - 1) & 1, 0x103)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t full = c.bar(B_F8_FULL + stage);
+          const uint32_t dst = c.sbase + OFF_F8 + stage * kF8StageBytes;
+          const int tok0 = (sg.tile_begin + jj) * kTileTokens;
+          mbar_arrive_expect_tx(full, kF8StageBytes);
+          for (int pc = 0; pc < pieces; ++pc) {
+            const int ptok = tok0 + pc * a.page_size;
+            int y = oob_row;
+            if (ptok < L) {
+              const int pid = bt[ptok / a.page_size];
+              if (pid >= 0 && pid < a.num_pages) y = pid * a.page_size;
+            }
+            const uint32_t rows = pc * a.page_size;
+            tma_load_2d(dst + rows * 256, tm_lat, full, 256 * rank, y);
+            tma_load_2d(dst + kF8RopeOff + rows * 32, tm_rope, full, 512 + 32 * rank, y);
+          }
+        }
+        __syncwarp();
+        continue;
+      }
       if (j >= kStages && !wait_bar_warp<false>(c, c.bar(B_KV_EMPTY + stage), ((j / kStages) - 1) & 1, 0x101)) {
         ok = false;
         break;
@@ -210,17 +260,96 @@ __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeA
   }
   // drain: the copies of the last stages must have landed before the CTA leaves
   const int issued = j;
+  const int landed_bar = F8 ? B_F8_FULL : B_KV_FULL;
   for (int k = issued - 1; k >= 0 && k >= issued - kStages; --k) {
     const long long t0 = clock64();
-    while (!mbar_try_wait(c.bar(B_KV_FULL + (k % kStages)), (k / kStages) & 1) && clock64() - t0 < kTimeoutCycles) {
+    while (!mbar_try_wait(c.bar(landed_bar + (k % kStages)), (k / kStages) & 1) && clock64() - t0 < kTimeoutCycles) {
     }
   }
 }
 
+// ------------------------------------------------------------------ e4m3 converter
+
+// Warps 2-3 (e4m3 cache only): expand each raw tile of the fp8 ring into an
+// fp16 operand stage laid out exactly like a bf16 stage (K-major 128B-swizzled
+// latent boxes, 64B-swizzled rope box), with cvt.rn.f16x2.e4m3x2 (exact:
+// every e4m3 value is an fp16 value).  Rows past the request's length are
+// written as zeros so 0-probability keys cannot inject NaN/Inf into P.V.
+// k_scale is not applied here: it is folded into the score scale and the
+// output scale.
+template <int CAP>
+__device__ void converter(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, int worker) {
+  const int w = (threadIdx.x >> 5) - 2;  // 0 or 1
+  const int lane = threadIdx.x & 31;
+  int j = 0;
+  bool ok = true;
+  for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
+    const Segment sg = sched.seg[s];
+    const int L = request_len(a, sg.req);
+    const int nt = segment_tiles(sg, L);
+    for (int jj = 0; jj < nt; ++jj, ++j) {
+      const int fs = j % kStages, os = j % kF8OpStages;
+      if (!wait_bar_warp<false>(c, c.bar(B_F8_FULL + fs), (j / kStages) & 1, 0x501)) { ok = false; break; }
+      if (j >= kF8OpStages &&
+          !wait_bar_warp<false>(c, c.bar(B_KV_EMPTY + os), ((j / kF8OpStages) - 1) & 1, 0x502)) {
+        ok = false;
+        break;
+      }
+      const int live = min(kTileTokens, L - (sg.tile_begin + jj) * kTileTokens);  // rows < live hold keys
+      const uint32_t src = c.sbase + OFF_F8 + fs * kF8StageBytes;
+      const uint32_t dst = c.sbase + OFF_KV + os * kStageBytes;
+      // latent: a warp converts one row per step, lane = 16-byte output chunk
+      // (8 keys' worth of bytes in, contiguous 256 B per warp read); eight
+      // rows' loads are issued before the first conversion so their shared
+      // memory latency overlaps
+      const int bx = lane >> 3, ch = lane & 7;
+#pragma unroll 1
+      for (int b8 = 0; b8 < kTileTokens / 16; ++b8) {
+        uint2 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 16 * b8 + 2 * i + w;
+          v[i] = r < live ? ld_shared_v2(src + r * 256 + lane * 8) : make_uint2(0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 16 * b8 + 2 * i + w;
+          const uint4 o = make_uint4(cvt_e4m3x2_f16x2(v[i].x), cvt_e4m3x2_f16x2(v[i].x >> 16),
+                                     cvt_e4m3x2_f16x2(v[i].y), cvt_e4m3x2_f16x2(v[i].y >> 16));
+          st_shared_v4(dst + bx * kLatBox + r * 128 + ((ch ^ (r & 7)) << 4), o);
+        }
+      }
+      // rope: 8 rows x 4 chunks per warp step
+      {
+        uint2 v[4];
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int r = 16 * it + 8 * w + (lane >> 2), cr = lane & 3;
+          v[it] = r < live ? ld_shared_v2(src + kF8RopeOff + r * 32 + cr * 8) : make_uint2(0, 0);
+        }
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int r = 16 * it + 8 * w + (lane >> 2), cr = lane & 3;
+          const uint4 o = make_uint4(cvt_e4m3x2_f16x2(v[it].x), cvt_e4m3x2_f16x2(v[it].x >> 16),
+                                     cvt_e4m3x2_f16x2(v[it].y), cvt_e4m3x2_f16x2(v[it].y >> 16));
+          st_shared_v4(dst + 4 * kLatBox + r * 64 + ((cr ^ ((r >> 1) & 3)) << 4), o);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(c.bar(B_KV_FULL + os));
+      mbar_arrive(c.bar(B_F8_EMPTY + fs));
+    }
+  }
+}
+
+
+
 // ------------------------------------------------------------------ MMA issuer
 
-template <int CAP>
+template <int CAP, bool F8>
 __device__ void mma_issuer(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, uint32_t tmem, int worker) {
+  constexpr int NS = op_stages<F8>();
+  constexpr uint32_t kIdescS = idesc_s<F8>(), kIdescPV = idesc_pv<F8>();
   // Two cursors walk this worker's tile sequence: S products run ahead as
   // soon as a cache tile has landed and the S buffer they write was read by
   // the softmax warps; P.V products follow as P tiles appear.  Whichever is
@@ -238,9 +367,9 @@ __device__ void mma_issuer(const Ctx& c, const Schedule<CAP>& sched, const Decod
   while (p_seg < seg_end) {
     bool progressed = false;
     if (s_seg < seg_end) {
-      const int stage = s_j % kStages;
+      const int stage = s_j % NS;
       bool ready = (s_jj > 0 || mbar_test_wait(c.bar(B_Q_READY), q_used & 1)) &&
-                   mbar_test_wait(c.bar(B_KV_FULL + stage), (s_j / kStages) & 1) &&
+                   mbar_test_wait(c.bar(B_KV_FULL + stage), (s_j / NS) & 1) &&
                    (s_j < 2 || mbar_test_wait(c.bar(B_S_FREE + (s_j & 1)), ((s_j >> 1) - 1) & 1));
       if (ready) {
         if (s_jj == 0) ++q_used;
@@ -271,7 +400,7 @@ __device__ void mma_issuer(const Ctx& c, const Schedule<CAP>& sched, const Decod
     }
     if (p_j < s_j && mbar_test_wait(c.bar(B_P_FULL), p_j & 1)) {
       tc_fence_after();
-      const uint32_t stage_addr = c.sbase + OFF_KV + (p_j % kStages) * kStageBytes;
+      const uint32_t stage_addr = c.sbase + OFF_KV + (p_j % NS) * kStageBytes;
       const uint32_t p_addr = c.sbase + OFF_P;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -283,7 +412,7 @@ __device__ void mma_issuer(const Ctx& c, const Schedule<CAP>& sched, const Decod
         mma_ss(tmem + TM_O, adesc, bdesc, kIdescPV, (p_jj == 0 && kk == 0) ? 0u : 1u);
       }
       mma_commit(c.bar(B_PV_DONE));
-      mma_commit(c.bar(B_KV_EMPTY + (p_j % kStages)));
+      mma_commit(c.bar(B_KV_EMPTY + (p_j % NS)));
       ++p_j;
       if (++p_jj == p_nt) {
         p_jj = 0;
@@ -325,7 +454,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& rlo, fl
 // into the peer CTA's receive buffer with st.async, which completes bytes on
 // the peer's x_full barrier.  Decoupled from the softmax warps so that the
 // ~0.5 us it takes to issue 32 KB of remote stores never blocks them.
-template <int CAP>
+// bf16 pair -> fp16 pair (exact for values in fp16's normal range, which
+// covers any sane query; used for the fp16 operands of the e4m3 path)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int CAP, bool F8>
 __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, uint32_t tmem, int worker,
                           int rank) {
   const int quad = (threadIdx.x >> 5) & 3;
@@ -353,7 +489,11 @@ __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const Decode
                                                         ((size_t)sg.req * M + row) * kRope + 32 * rank);
       uint4 rp[4];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) rp[ch] = valid_row ? __ldg(srp + ch) : make_uint4(0, 0, 0, 0);
+      for (int ch = 0; ch < 4; ++ch) {
+        rp[ch] = valid_row ? __ldg(srp + ch) : make_uint4(0, 0, 0, 0);
+        if (F8) rp[ch] = make_uint4(bf16x2_to_f16x2(rp[ch].x), bf16x2_to_f16x2(rp[ch].y), bf16x2_to_f16x2(rp[ch].z),
+                                    bf16x2_to_f16x2(rp[ch].w));
+      }
       // two rounds of 16 independent 16-byte loads (one latency each)
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
@@ -368,13 +508,16 @@ __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const Decode
             r[4 * v + 0] = q[8 * ck + v].x; r[4 * v + 1] = q[8 * ck + v].y;
             r[4 * v + 2] = q[8 * ck + v].z; r[4 * v + 3] = q[8 * ck + v].w;
           }
+          if (F8) {
+#pragma unroll
+            for (int v = 0; v < 32; ++v) r[v] = bf16x2_to_f16x2(r[v]);
+          }
           tmem_st32(tmem + lane_off + TM_Q + 64 * hh + 32 * ck, r);
         }
       }
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch)
         st_shared_v4(c.sbase + OFF_QROPE + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4), rp[ch]);
-      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(c.bar(B_Q_READY));
@@ -383,11 +526,8 @@ __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const Decode
       const int sb = j & 1, u = j >> 1;
       if (!wait_bar_warp<false>(c, c.bar(B_S_FULL + sb), u & 1, 0x401)) { ok = false; break; }
       tc_fence_after();
-      uint32_t s0[32], s1[32];
-      tmem_ld32(tmem + lane_off + TM_S + 64 * sb, s0);
-      tmem_ld32(tmem + lane_off + TM_S + 64 * sb + 32, s1);
-      tmem_ld_wait(s0);
-      tmem_ld_wait(s1);
+      uint32_t sv64[64];
+      tmem_ld64(tmem + lane_off + TM_S + 64 * sb, sv64);
       tc_fence_before();
       mbar_arrive(c.bar(B_S_LOADED + sb));
       // the two 32-key halves go to ring slots (2j) % 3 and (2j + 1) % 3;
@@ -398,7 +538,7 @@ __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const Decode
         if (ug > 0 && !wait_bar_warp<true>(c, c.bar(B_X_EMPTY + k), (ug - 1) & 1, 0x402)) { ok = false; break; }
         const uint32_t dst = xchg_peer + k * kSlotBytes;
         const uint32_t mb = x_full_peer + 8 * k;
-        const uint32_t* sv = h ? s1 : s0;
+        const uint32_t* sv = sv64 + 32 * h;
         if (valid_row) {
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch)
@@ -410,9 +550,14 @@ __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const Decode
       if (!ok) break;
     }
   }
+  // drain: the peer's notes for the last half tiles are the only remote
+  // writes nothing else waits for; they must land before this CTA may exit
+  // (half tile g sits in slot g % kSlots, phase g / kSlots)
+  for (int g = 2 * j - 1; ok && g >= 0 && g >= 2 * j - kSlots; --g)
+    if (!wait_bar_warp<true>(c, c.bar(B_X_EMPTY + g % kSlots), (g / kSlots) & 1, 0x403)) break;
 }
 
-template <int CAP>
+template <int CAP, bool F8>
 __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, uint32_t tmem,
                                  int worker, int rank) {
   // Two warps per TMEM lane quadrant: warp (4 + q) and (8 + q) own query rows
@@ -457,7 +602,6 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
         tc_fence_after();
         uint32_t cur[32];
         tmem_ld32(tmem + lane_off + TM_S + 64 * sb + 32 * half, cur);
-        tmem_ld_wait(cur);
         tc_fence_before();
         mbar_arrive(c.bar(B_S_FREE + sb));  // the MMA may overwrite this S buffer
         // ---- full scores: own partial + the peer's (its st.async bytes
@@ -520,12 +664,10 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
             uint32_t o[32];
             const uint32_t addr = tmem + lane_off + TM_O + 128 * half + 32 * ck;
             tmem_ld32(addr, o);
-            tmem_ld_wait(o);
 #pragma unroll
             for (int v = 0; v < 32; ++v) o[v] = __float_as_uint(__uint_as_float(o[v]) * alpha);
             tmem_st32(addr, o);
           }
-          tmem_st_wait();
         }
         if (resc) {
           l *= alpha;
@@ -540,8 +682,13 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
         for (int k = 0; k < 16; ++k) {
           const float p0 = ex2_approx(fmaf(x[2 * k], cs, nm));
           const float p1 = ex2_approx(fmaf(x[2 * k + 1], cs, nm));
-          float r0, r1;
-          pk[k] = pack_bf16(p0, p1, r0, r1);
+          if (F8) {
+            __half2 hv = __floats2half2_rn(p0, p1);
+            pk[k] = *reinterpret_cast<uint32_t*>(&hv);
+          } else {
+            float r0, r1;
+            pk[k] = pack_bf16(p0, p1, r0, r1);
+          }
           lsum += p0 + p1;  // l from the unrounded probabilities: exact lse
         }
         l += lsum;
@@ -580,7 +727,6 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
         uint32_t o[32];
         if (nt > 0) {
           tmem_ld32(tmem + lane_off + TM_O + 128 * half + 32 * ck, o);
-          tmem_ld_wait(o);
         }
         if (nt == 0 || !live) {
 #pragma unroll
@@ -622,7 +768,7 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
 
 // ------------------------------------------------------------------ kernel
 
-template <int CAP>
+template <int CAP, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ Schedule<CAP> sched, const __grid_constant__ DecodeArgs a,
                   const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope) {
@@ -640,8 +786,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *c.abort_flag = 0;
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(c.bar(B_KV_FULL + s), 1);
+      mbar_init(c.bar(B_KV_FULL + s), F8 ? 64 : 1);  // e4m3: the 64 converter threads
       mbar_init(c.bar(B_KV_EMPTY + s), 1);
+      mbar_init(c.bar(B_F8_FULL + s), 1);
+      mbar_init(c.bar(B_F8_EMPTY + s), 64);
     }
     for (int i = 0; i < 2; ++i) mbar_init(c.bar(B_S_FULL + i), 1);
     mbar_init(c.bar(B_P_FULL), 256);
@@ -676,14 +824,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (worker < sched.num_workers) {
     if (warp == 0) {
-      producer<CAP>(c, sched, a, &tm_lat, &tm_rope, worker, rank);
+      producer<CAP, F8>(c, sched, a, &tm_lat, &tm_rope, worker, rank);
     } else if (warp == 1) {
-      if ((threadIdx.x & 31) == 0) mma_issuer<CAP>(c, sched, a, tmem, worker);
+      if ((threadIdx.x & 31) == 0) mma_issuer<CAP, F8>(c, sched, a, tmem, worker);
       __syncwarp();
     } else if (warp >= 12) {
-      exchanger<CAP>(c, sched, a, tmem, worker, rank);
+      exchanger<CAP, F8>(c, sched, a, tmem, worker, rank);
     } else if (warp >= 4) {
-      softmax_epilogue<CAP>(c, sched, a, tmem, worker, rank);
+      softmax_epilogue<CAP, F8>(c, sched, a, tmem, worker, rank);
+    } else if (F8) {
+      converter<CAP>(c, sched, a, worker);
     }
   }
 
@@ -710,28 +860,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D view [num_pages * page_size rows, 576 columns] of the cache.
+// 2-D view [num_pages * page_size rows, 576 columns] of the cache (bf16 or
+// one-byte e4m3 elements).
 static bool make_map(CUtensorMap* m, const void* kv, int64_t rows, int box_cols, int box_rows,
-                     CUtensorMapSwizzle sw) {
+                     CUtensorMapSwizzle sw, bool fp8) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kKvDim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kKvDim * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)kKvDim * (fp8 ? 1 : 2)};
   cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims, strides, box, estr,
+  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(kv), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int CAP>
+template <int CAP, bool F8>
 static cudaError_t launch_cap(const mla_plan& p, const DecodeArgs& a, const CUtensorMap& lat,
                               const CUtensorMap& rope, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(decode_kernel<CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr_err =
+        cudaFuncSetAttribute(decode_kernel<CAP, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   Schedule<CAP> s;
@@ -739,21 +892,32 @@ static cudaError_t launch_cap(const mla_plan& p, const DecodeArgs& a, const CUte
   s.num_segments = (int32_t)p.segs.size();
   for (int w = 0; w <= p.num_workers; ++w) s.worker_seg[w] = p.worker_seg[w];
   for (size_t i = 0; i < p.segs.size(); ++i) s.seg[i] = p.segs[i];
-  decode_kernel<CAP><<<dim3(2 * p.num_workers), kThreads, kSmemBytes, stream>>>(s, a, lat, rope);
+  decode_kernel<CAP, F8><<<dim3(2 * p.num_workers), kThreads, kSmemBytes, stream>>>(s, a, lat, rope);
   return cudaGetLastError();
+}
+
+template <bool F8>
+static cudaError_t launch_dtype(const mla_plan& p, const DecodeArgs& a, cudaStream_t stream) {
+  CUtensorMap lat, rope;
+  const int64_t rows = a.num_pages * a.page_size;
+  // bf16: four 64-column 128B-swizzled latent boxes + one 32-column 64B-swizzled
+  // rope box per page piece; e4m3: one raw 256-byte latent box + one 32-byte
+  // rope box, unswizzled (the converter warps lay out the operands)
+  const bool ok = F8 ? make_map(&lat, a.kv, rows, 256, a.page_size, CU_TENSOR_MAP_SWIZZLE_NONE, true) &&
+                           make_map(&rope, a.kv, rows, 32, a.page_size, CU_TENSOR_MAP_SWIZZLE_NONE, true)
+                     : make_map(&lat, a.kv, rows, 64, a.page_size, CU_TENSOR_MAP_SWIZZLE_128B, false) &&
+                           make_map(&rope, a.kv, rows, 32, a.page_size, CU_TENSOR_MAP_SWIZZLE_64B, false);
+  if (!ok) return cudaErrorNotSupported;
+  if (p.segs.size() <= (size_t)kSegCapSmall) return launch_cap<kSegCapSmall, F8>(p, a, lat, rope, stream);
+  return launch_cap<kSegCapLarge, F8>(p, a, lat, rope, stream);
 }
 
 }  // namespace sm103
 
 // Returns cudaErrorNotSupported when the tensor-map encoder is unavailable.
 cudaError_t launch_sm103(const mla_plan& p, const DecodeArgs& a, cudaStream_t stream) {
-  CUtensorMap lat, rope;
-  const int64_t rows = a.num_pages * a.page_size;
-  if (!sm103::make_map(&lat, a.kv, rows, 64, a.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !sm103::make_map(&rope, a.kv, rows, 32, a.page_size, CU_TENSOR_MAP_SWIZZLE_64B))
-    return cudaErrorNotSupported;
-  if (p.segs.size() <= (size_t)kSegCapSmall) return sm103::launch_cap<kSegCapSmall>(p, a, lat, rope, stream);
-  return sm103::launch_cap<kSegCapLarge>(p, a, lat, rope, stream);
+  return a.kv_dtype == MLA_KV_E4M3 ? sm103::launch_dtype<true>(p, a, stream)
+                                   : sm103::launch_dtype<false>(p, a, stream);
 }
 
 // Kernel-side error code recorded since the last reset (0 = none).

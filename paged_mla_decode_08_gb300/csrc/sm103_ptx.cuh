@@ -186,40 +186,53 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 
 #define MLA_R8(b) "=r"(r[b + 0]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), "=r"(r[b + 4]), "=r"(r[b + 5]), \
                   "=r"(r[b + 6]), "=r"(r[b + 7])
-#define MLA_P8(b) "+r"(r[b + 0]), "+r"(r[b + 1]), "+r"(r[b + 2]), "+r"(r[b + 3]), "+r"(r[b + 4]), "+r"(r[b + 5]), \
-                  "+r"(r[b + 6]), "+r"(r[b + 7])
 #define MLA_I8(b) "r"(r[b + 0]), "r"(r[b + 1]), "r"(r[b + 2]), "r"(r[b + 3]), "r"(r[b + 4]), "r"(r[b + 5]), \
                   "r"(r[b + 6]), "r"(r[b + 7])
 
+// TMEM loads and stores.  Each load is issued together with its
+// tcgen05.wait::ld in ONE asm statement, so the compiler sees the destination
+// registers defined only once the data is there: no copy, spill or reuse of
+// those registers can fall between the asynchronous load and its wait.
+// Likewise each store is followed by its tcgen05.wait::st in the same
+// statement, so its source registers stay untouched until TMEM holds them.
+//
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane
-// (lane base of taddr) + t.  The values are valid after tmem_ld_wait(r).
+// (lane base of taddr) + t, register i = column i.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31"
+      "}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : MLA_R8(0), MLA_R8(8), MLA_R8(16), MLA_R8(24)
-      : "r"(taddr));
+      : "r"(taddr)
+      : "memory");
 }
-// Wait for this thread's tcgen05.ld; ties the registers so no use is
-// scheduled before the wait.
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : MLA_P8(0), MLA_P8(8), MLA_P8(16), MLA_P8(24)::"memory");
+// 32 lanes x 64 consecutive columns in one load.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63"
+      "}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : MLA_R8(0), MLA_R8(8), MLA_R8(16), MLA_R8(24), MLA_R8(32), MLA_R8(40), MLA_R8(48), MLA_R8(56)
+      : "r"(taddr)
+      : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {"
+      "%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32"
+      "};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
       MLA_I8(0), MLA_I8(8), MLA_I8(16), MLA_I8(24)
       : "memory");
 }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16};" ::"r"(taddr),
-      MLA_I8(0), MLA_I8(8)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
@@ -233,7 +246,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 #undef MLA_R8
-#undef MLA_P8
 #undef MLA_I8
 
 // ---------------------------------------------------------------- descriptors
@@ -252,12 +264,25 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator, bf16
-// A and B, A/B major-ness (0 = K-major, 1 = MN-major), N >> 3, M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
+// Instruction descriptor of tcgen05.mma.kind::f16: fp32 accumulator, A and B
+// both bf16 (fmt 1) or both fp16 (fmt 0), A/B major-ness (0 = K-major,
+// 1 = MN-major), N >> 3, M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int a_mn_major, int b_mn_major, uint32_t fmt) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
          (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Two float8 e4m3 values (low / high byte of `v`) -> two fp16, exactly.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t v) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(d) : "r"(v));
+  return d;
+}
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
 }
 
 }  // namespace ptx
