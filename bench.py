@@ -304,7 +304,7 @@ def our_arm(args, w, rank, world):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3-kv/bf16-mma",
+        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3-kv/fp16-mma",
         "data": "synthetic", "config": workload_desc(w),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": profiled_traffic(w.name),
