@@ -209,6 +209,20 @@ def reference_arm(args, w, rank):
 # ------------------------------------------------------------------ GPU arm
 
 
+def whole_job_rate(my_seconds, tokens_per_step, steps, world, dist=None, device=None):
+    """Weak-scaling aggregate over replicas: every rank decodes its own copy
+    of the workload for `steps` steps; the job's time is the slowest rank's
+    (all-reduce MAX) and its tokens are all ranks' tokens.  Returns
+    (tokens/s of the whole job, the job's seconds)."""
+    import torch
+    t = my_seconds
+    if dist is not None and world > 1:
+        buf = torch.tensor([my_seconds], dtype=torch.float64, device=device)
+        dist.all_reduce(buf, op=dist.ReduceOp.MAX)
+        t = float(buf.item())
+    return tokens_per_step * steps * world / t, t
+
+
 def our_arm(args, w, rank, world):
     import torch
     from paged_mla_decode_08_gb300 import binding as B
@@ -272,13 +286,7 @@ def our_arm(args, w, rank, world):
     main_ms = [e[0].elapsed_time(e[1]) for e in ev]
     comb_ms = [e[1].elapsed_time(e[2]) for e in ev]
     step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    tot_s = sum(step_ms) / 1e3
-    if dist:
-        t = torch.tensor([tot_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_s = float(t.item())
-    tokens = st["tokens"] * K * world
-    value = tokens / tot_s
+    value, tot_s = whole_job_rate(sum(step_ms) / 1e3, st["tokens"], K, world, dist, dev)
     ms_per_step = tot_s * 1e3 / K
 
     # ---- e2e: host buffers in, results back to the host, copies timed
