@@ -179,7 +179,7 @@ int mla_decode_combine(const mla_plan* plan, void* out, float* lse, void* worksp
  *   - The first call on a device looks up the array's device address once;
  *     make that call before any stream capture.
  */
-#define MLA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+#define MLA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int mla_decode_noalloc(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_tokens,
                        int num_heads, const void* kv_pages, int kv_dtype, int64_t num_pages,
                        int page_size, const int32_t* block_table, int bt_stride,

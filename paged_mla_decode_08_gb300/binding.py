@@ -184,7 +184,7 @@ def mla_decode_noalloc(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_
     _check(load().mla_decode_noalloc(*args[:16], args[18]))
 
 
-MLA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+MLA_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 def mla_planner_constants():

@@ -99,7 +99,7 @@ int prepare(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_
   a.q_nope = q_nope; a.q_pe = q_pe; a.kv = kv_pages;
   a.block_table = block_table; a.seq_lens = seq_lens;
   a.out = out; a.lse = lse;
-  a.part_o = static_cast<float*>(workspace);
+  a.part_o = workspace;
   a.part_lse = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan->ws_lse_offset) : nullptr;
   a.num_pages = num_pages; a.page_size = page_size; a.kv_dtype = kv_dtype; a.bt_stride = bt_stride;
   a.batch = plan->batch; a.q_len = plan->q_len; a.num_heads = plan->num_heads; a.rows = plan->rows;
@@ -185,7 +185,7 @@ int mla_decode_combine(const mla_plan* plan, void* out, float* lse, void* worksp
   std::memset(&pr, 0, sizeof(pr));
   mla::DecodeArgs& a = pr.args;
   a.out = out; a.lse = lse;
-  a.part_o = static_cast<float*>(workspace);
+  a.part_o = workspace;
   a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan->ws_lse_offset);
   a.batch = plan->batch; a.q_len = plan->q_len; a.num_heads = plan->num_heads; a.rows = plan->rows;
   rc = launch_combine(plan, pr, static_cast<cudaStream_t>(stream));

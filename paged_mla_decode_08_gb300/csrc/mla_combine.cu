@@ -9,15 +9,18 @@
 // of the pages (sglang trtllm_mla_backend.py, forward_extend: fixed-up rows
 // with lse = -inf so the merge ignores them).
 //
-// Partials are chunk-major, part_o[slot][c][row] (c = 16-byte chunk of 4
-// output columns), so that the producing kernels store coalesced.  One CTA of
-// 256 threads per (job, block of 32 query rows, quarter of the 128 chunks):
-// the split weights e^{lse_s - lse} of the 32 rows go to shared memory, then
-// a warp owns 4 chunks and reads them for 32 consecutive rows (512
-// contiguous bytes per chunk and split, four independent loads in flight),
-// and the 32 x 128 bf16 result is transposed through shared memory so that
-// each output row segment is written with contiguous 16-byte stores.
-// Memory bound: nsplit * 2 KB read + 1 KB written per row.
+// Partials are bf16 and chunk-major, part_o[slot][c][row] (c = 16-byte chunk
+// of 8 output columns), so that the producing kernel stores coalesced.  One
+// CTA of 256 threads per (job, block of 32 query rows, quarter of the 64
+// chunks): a warp owns 2 chunks and reads them for 32 consecutive rows (512
+// contiguous bytes per chunk and split); the partials of the first four
+// splits are requested before the split weights e^{lse_s - lse} are computed
+// (one warp, into shared memory), so both memory latencies overlap; the
+// 32 x 128 bf16 result is transposed through shared memory so that each
+// output row segment is written with contiguous 16-byte stores.  The bf16
+// partials add one rounding of O_s (relative 2^-9) before the merge, well
+// inside the output tolerance, and halve the bytes written and read.
+// Memory bound: nsplit * 1 KB read + 1 KB written per row.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -26,7 +29,12 @@
 namespace mla {
 
 constexpr int kCombRows = 32;
-constexpr int kCombChunks = 32;  // per CTA: a quarter of the 128 chunks
+constexpr int kChunkCols = 8;                  // a 16-byte chunk of bf16 partial outputs
+constexpr int kChunks = kLatent / kChunkCols;  // 64 per row
+constexpr int kCombChunks = kChunks / 4;       // per CTA: a quarter of the row
+
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
 template <int CAP>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineList<CAP> jobs,
@@ -37,64 +45,90 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
   const int r0 = blockIdx.y * kCombRows;
   const int c0 = blockIdx.z * kCombChunks;
   const int nrows = min(kCombRows, M - r0);
-  __shared__ uint2 s_out[kCombRows][kCombChunks + 1];
+  __shared__ uint4 s_out[kCombRows][kCombChunks + 1];
+
+  const int r = threadIdx.x & 31;  // row within the block
+  const int cw = threadIdx.x >> 5;  // warp: chunks c0 + cw + 8k, k < 2
+  const uint4* po = reinterpret_cast<const uint4*>(a.part_o) + ((size_t)job.slot_begin * kChunks + c0 + cw) * M + r0 + r;
+  const size_t split_stride = (size_t)kChunks * M;
+  // The partials of the first kGroup splits do not depend on the weights:
+  // their loads go out before the lse values are even read, so the two
+  // memory round trips overlap.
+  constexpr int kGroup = 4;
+  uint4 v[kGroup][2];
+#pragma unroll
+  for (int g = 0; g < kGroup; ++g)
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      v[g][k] = (r < nrows && g < job.nsplit) ? __ldg(po + g * split_stride + (size_t)(8 * k) * M) : make_uint4(0, 0, 0, 0);
 
   if (threadIdx.x < kCombRows) {
-    const int r = threadIdx.x;
     float mx = -CUDART_INF_F, tot = 0.f;
     const float* pl = a.part_lse + (size_t)job.slot_begin * M + r0 + r;
     if (r < nrows) {
-      for (int s = 0; s < job.nsplit; ++s) mx = fmaxf(mx, pl[(size_t)s * M]);
+      for (int s = 0; s < job.nsplit; ++s) mx = fmaxf(mx, __ldg(pl + (size_t)s * M));
       if (mx != -CUDART_INF_F)
-        for (int s = 0; s < job.nsplit; ++s) tot += __expf(pl[(size_t)s * M] - mx);
+        for (int s = 0; s < job.nsplit; ++s) tot += __expf(__ldg(pl + (size_t)s * M) - mx);
       if (blockIdx.z == 0) a.lse[(size_t)job.req * M + r0 + r] = tot > 0.f ? mx + __logf(tot) : -CUDART_INF_F;
     }
     const float inv = tot > 0.f ? 1.f / tot : 0.f;
     for (int s = 0; s < job.nsplit; ++s) {
-      const float l = r < nrows ? pl[(size_t)s * M] : -CUDART_INF_F;
+      const float l = r < nrows ? __ldg(pl + (size_t)s * M) : -CUDART_INF_F;
       s_w[s * kCombRows + r] = (inv > 0.f && l != -CUDART_INF_F) ? __expf(l - mx) * inv : 0.f;
     }
   }
   __syncthreads();
 
-  const int r = threadIdx.x & 31;  // row within the block
-  const int cw = threadIdx.x >> 5;  // warp: chunks c0 + cw + 8k, k < 4
-  float4 acc[4];
+  float acc[2][8];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[k][e] = 0.f;
   if (r < nrows) {
-    const float4* po = reinterpret_cast<const float4*>(a.part_o) +
-                       ((size_t)job.slot_begin * (kLatent / 4) + c0 + cw) * M + r0 + r;
-    const size_t split_stride = (size_t)(kLatent / 4) * M;
-    for (int s = 0; s < job.nsplit; ++s) {
-      const float wgt = s_w[s * kCombRows + r];
-      if (wgt == 0.f) continue;
-      float4 v[4];
+    for (int s0 = 0; s0 < job.nsplit; s0 += kGroup) {
+      if (s0 > 0) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = __ldg(po + s * split_stride + (size_t)(8 * k) * M);
+        for (int g = 0; g < kGroup; ++g)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc[k].x = fmaf(wgt, v[k].x, acc[k].x);
-        acc[k].y = fmaf(wgt, v[k].y, acc[k].y);
-        acc[k].z = fmaf(wgt, v[k].z, acc[k].z);
-        acc[k].w = fmaf(wgt, v[k].w, acc[k].w);
+          for (int k = 0; k < 2; ++k)
+            v[g][k] = s0 + g < job.nsplit ? __ldg(po + (s0 + g) * split_stride + (size_t)(8 * k) * M)
+                                          : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        // a split with weight 0 (lse = -inf, or past nsplit) adds nothing;
+        // its partial may hold anything, so it is skipped, not multiplied
+        const float wgt = s0 + g < job.nsplit ? s_w[(s0 + g) * kCombRows + r] : 0.f;
+        if (wgt == 0.f) continue;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t w4[4] = {v[g][k].x, v[g][k].y, v[g][k].z, v[g][k].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[k][2 * e] = fmaf(wgt, bf_lo(w4[e]), acc[k][2 * e]);
+            acc[k][2 * e + 1] = fmaf(wgt, bf_hi(w4[e]), acc[k][2 * e + 1]);
+          }
+        }
       }
     }
   }
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z, acc[k].w);
-    s_out[r][cw + 8 * k] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  for (int k = 0; k < 2; ++k) {
+    uint32_t q[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(acc[k][2 * e], acc[k][2 * e + 1]);
+      q[e] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    s_out[r][cw + 8 * k] = make_uint4(q[0], q[1], q[2], q[3]);
   }
   __syncthreads();
   // 32 rows x 256 bytes: a half-warp writes one row segment (16 lanes x 16 B)
   const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
   for (int rr = hw; rr < nrows; rr += 16) {
     const size_t row = (size_t)job.req * M + r0 + rr;
-    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * kLatent + 4 * c0) + l16;
-    const uint2 x0 = s_out[rr][2 * l16], x1 = s_out[rr][2 * l16 + 1];
-    *dst = make_uint4(x0.x, x0.y, x1.x, x1.y);
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * kLatent + kChunkCols * c0) + l16;
+    *dst = s_out[rr][l16];
   }
 }
 
@@ -108,7 +142,7 @@ static cudaError_t launch_combine_cap(const std::vector<CombineJob>& jobs, const
   for (const CombineJob& j : jobs) maxsplit = j.nsplit > maxsplit ? j.nsplit : maxsplit;
   const size_t smem = (size_t)maxsplit * kCombRows * sizeof(float);  // <= 128 splits: 16 KB
   combine_kernel<CAP><<<dim3((unsigned)jobs.size(), (unsigned)((a.rows + kCombRows - 1) / kCombRows),
-                             (unsigned)(kLatent / 4 / kCombChunks)),
+                             (unsigned)(kChunks / kCombChunks)),
                         256, smem, stream>>>(list, a);
   return cudaGetLastError();
 }

@@ -64,7 +64,7 @@ struct DecodeArgs {
   const int32_t* seq_lens;
   void* out;           // bf16 [T, H, 512]
   float* lse;          // fp32 [T, H]
-  float* part_o;       // fp32 [slots, M, 512]  (O / l of one split)
+  void* part_o;        // bf16 [slot][64 chunks of 8 columns][M] (O / l of one split)
   float* part_lse;     // fp32 [slots, M]
   int64_t num_pages;
   int32_t page_size;

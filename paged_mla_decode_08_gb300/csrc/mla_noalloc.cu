@@ -10,7 +10,8 @@
 // in this file as a statically sized __device__ variable instead.
 //
 // Cost and limits.
-//  - The array is MLA_NOALLOC_SCRATCH_BYTES (32 MiB).  It is part of the
+//  - The array is MLA_NOALLOC_SCRATCH_BYTES (16 MiB: 127 split slots of 128
+//    query rows with bf16 partials).  It is part of the
 //    library's device image, so a device holds it from the moment this code is
 //    loaded on it until the process exits.
 //  - A plan whose workspace size exceeds the array is rejected with
@@ -75,7 +76,7 @@ extern "C" int mla_decode_noalloc(const mla_plan* plan, const void* q_nope, cons
   if (!plan) return mla::report_error(MLA_ERR_ARG, "plan is NULL");
   if (mla_plan_workspace_bytes(plan) > (size_t)MLA_NOALLOC_SCRATCH_BYTES)
     return mla::report_error(MLA_ERR_WORKSPACE,
-                             "mla_decode_noalloc: the plan needs more scratch than the built-in 32 MiB "
+                             "mla_decode_noalloc: the plan needs more scratch than the built-in 16 MiB "
                              "(mla_plan_workspace_bytes); call mla_decode with a caller workspace instead");
   int rc = MLA_OK;
   void* ws = scratch_address(&rc);

@@ -128,7 +128,7 @@ int build_plan(const int32_t* seq_lens, int batch, int page_size, int num_heads,
   for (int i = 0; i < (int)p->segs.size(); ++i) p->worker_seg[p->seg_worker[i] + 1] = i + 1;
   for (int i = 1; i <= W; ++i) p->worker_seg[i] = std::max(p->worker_seg[i], p->worker_seg[i - 1]);
 
-  const size_t o_bytes = (size_t)slots * p->rows * kLatent * sizeof(float);
+  const size_t o_bytes = (size_t)slots * p->rows * kLatent * 2;  // bf16 partial outputs
   p->ws_lse_offset = (o_bytes + 255) / 256 * 256;
   const size_t l_bytes = (size_t)slots * p->rows * sizeof(float);
   p->ws_bytes = slots ? p->ws_lse_offset + (l_bytes + 255) / 256 * 256 : 0;

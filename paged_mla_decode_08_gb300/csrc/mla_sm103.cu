@@ -465,7 +465,8 @@ template <int CAP, bool F8>
 __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, uint32_t tmem, int worker,
                           int rank) {
   const int quad = (threadIdx.x >> 5) & 3;
-  const int row = quad * 32 + (threadIdx.x & 31);
+  const int lane = threadIdx.x & 31;
+  const int row = quad * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   const uint32_t peer = rank ^ 1;
   const uint32_t xchg_peer = mapa(c.sbase + OFF_XCHG, peer) + row * 16;
@@ -480,44 +481,72 @@ __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const Decode
     if (nt == 0) continue;
     // ---- this segment's query: latent half -> TMEM columns [384, 512), rope
     // half -> shared memory (64B swizzle).  The previous segment's S MMAs all
-    // completed (this warp waited for each), so the old Q is dead; the load
-    // overlaps the softmax warps' last tile and epilogue.
+    // completed (this warp waited for each), so the old Q and the rope area
+    // are dead; the load overlaps the softmax warps' last tile and epilogue.
+    // Loads are coalesced: four lanes read one 64-byte piece of a row, eight
+    // rows per instruction.  Each 64-byte column piece of the warp's 32 rows
+    // is staged through this warp's 2 KB of the rope area (XOR-swizzled by
+    // row pair, conflict-free both ways) so that lane r can store row r's
+    // piece into TMEM; the rope rows go straight to their final layout.
     {
-      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q_nope) +
-                                                        ((size_t)sg.req * M + row) * kLatent + 256 * rank);
-      const uint4* srp = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q_pe) +
-                                                        ((size_t)sg.req * M + row) * kRope + 32 * rank);
-      uint4 rp[4];
+      const int ql = lane >> 2, qc = lane & 3;  // load mapping: row 8k + ql, 16-byte chunk qc
+      const size_t row0 = (size_t)sg.req * M + 32 * quad;
+      const uint4* qn = reinterpret_cast<const uint4*>(a.q_nope) + row0 * (kLatent / 8) + 32 * rank + qc;
+      const uint4* qp = reinterpret_cast<const uint4*>(a.q_pe) + row0 * (kRope / 8) + 4 * rank + qc;
+      const uint32_t stage = c.sbase + OFF_QROPE + quad * 2048;  // this warp's rows of the rope area
+      auto lrow_ok = [&](int rl) { return 32 * quad + rl < M; };
+      auto cvt4 = [&](uint4 v) {
+        return F8 ? make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w))
+                  : v;
+      };
+      uint4 rpe[4], lat[4][4];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        rp[ch] = valid_row ? __ldg(srp + ch) : make_uint4(0, 0, 0, 0);
-        if (F8) rp[ch] = make_uint4(bf16x2_to_f16x2(rp[ch].x), bf16x2_to_f16x2(rp[ch].y), bf16x2_to_f16x2(rp[ch].z),
-                                    bf16x2_to_f16x2(rp[ch].w));
-      }
-      // two rounds of 16 independent 16-byte loads (one latency each)
-#pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        uint4 q[16];
+      for (int rd = 0; rd < 4; ++rd)
 #pragma unroll
-        for (int v = 0; v < 16; ++v) q[v] = valid_row ? __ldg(src + hh * 16 + v) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int ck = 0; ck < 2; ++ck) {
-          uint32_t r[32];
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            r[4 * v + 0] = q[8 * ck + v].x; r[4 * v + 1] = q[8 * ck + v].y;
-            r[4 * v + 2] = q[8 * ck + v].z; r[4 * v + 3] = q[8 * ck + v].w;
-          }
-          if (F8) {
-#pragma unroll
-            for (int v = 0; v < 32; ++v) r[v] = bf16x2_to_f16x2(r[v]);
-          }
-          tmem_st32(tmem + lane_off + TM_Q + 64 * hh + 32 * ck, r);
+        for (int k = 0; k < 4; ++k) {
+          const int rl = 8 * k + ql;
+          lat[rd][k] = lrow_ok(rl) ? __ldg(qn + (size_t)rl * (kLatent / 8) + 4 * rd) : make_uint4(0, 0, 0, 0);
         }
-      }
+      // piece p (0..7) = latent columns [32p, 32p+32) of this CTA's half =
+      // TMEM columns TM_Q + 16p; piece p + 4 is requested as piece p retires
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
-        st_shared_v4(c.sbase + OFF_QROPE + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4), rp[ch]);
+      for (int pc = 0; pc < 8; ++pc) {
+        const int rd = pc & 3;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int rl = 8 * k + ql;
+          st_shared_v4(stage + rl * 64 + ((qc ^ ((rl >> 1) & 3)) << 4), lat[rd][k]);
+        }
+        __syncwarp();
+        if (pc < 4) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rl = 8 * k + ql;
+            lat[rd][k] = lrow_ok(rl) ? __ldg(qn + (size_t)rl * (kLatent / 8) + 4 * (rd + 4)) : make_uint4(0, 0, 0, 0);
+          }
+        } else if (pc == 4) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rl = 8 * k + ql;
+            rpe[k] = lrow_ok(rl) ? __ldg(qp + (size_t)rl * (kRope / 8)) : make_uint4(0, 0, 0, 0);
+          }
+        }
+        uint32_t r[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 v = cvt4(ld_shared_v4(stage + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4)));
+          r[4 * i + 0] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+        }
+        tmem_st16(tmem + lane_off + TM_Q + 16 * pc, r);
+        __syncwarp();
+      }
+      // rope rows of this warp in the MMA's 64B-swizzled layout (row-pair
+      // XOR of the 16-byte chunk: the same pattern as the staging)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int rl = 8 * k + ql;
+        st_shared_v4(stage + rl * 64 + ((qc ^ ((rl >> 1) & 3)) << 4), cvt4(rpe[k]));
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(c.bar(B_Q_READY));
@@ -747,13 +776,19 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
             dst[v] = w;
           }
         } else {
-          // partials are chunk-major, [slot][16-byte chunk][row]: a warp's
-          // 32 rows store 512 contiguous bytes
-          float4* dst = reinterpret_cast<float4*>(a.part_o) + ((size_t)sg.slot * (kLatent / 4) + col / 4) * M + row;
+          // partials are bf16, chunk-major [slot][8-column chunk][row]: a
+          // warp's 32 rows store 512 contiguous bytes per chunk
+          uint4* dst = reinterpret_cast<uint4*>(a.part_o) + ((size_t)sg.slot * (kLatent / 8) + col / 8) * M + row;
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[(size_t)v * M] = make_float4(__uint_as_float(o[4 * v + 0]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                             __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+          for (int v = 0; v < 4; ++v) {
+            float d0, d1;
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv, d0, d1);
+            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv, d0, d1);
+            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv, d0, d1);
+            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv, d0, d1);
+            dst[(size_t)v * M] = w;
+          }
         }
       }
       if (rank == 0 && half == 0 && valid_row) {

@@ -233,6 +233,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       MLA_I8(0), MLA_I8(8), MLA_I8(16), MLA_I8(24)
       : "memory");
 }
+// 32 lanes x 16 consecutive columns, followed by its wait.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {"
+      "%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16"
+      "};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      MLA_I8(0), MLA_I8(8)
+      : "memory");
+}
 
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {

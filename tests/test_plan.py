@@ -121,7 +121,7 @@ def test_plan_matches_rule(name, sms):
     check_invariants(segs, lens, sms // 2, tile, slots)
     rows = cfg["num_heads"] * cfg["q_len"]
     if slots:
-        o = slots * rows * 512 * 4
+        o = slots * rows * 512 * 2
         want_ws = -(-o // 256) * 256 + -(-(slots * rows * 4) // 256) * 256
     else:
         want_ws = 0

@@ -57,7 +57,7 @@ def test_noalloc_matches_workspace_decode_twice():
 
 def test_noalloc_rejects_plan_larger_than_scratch():
     lens = np.full(256, 8192, dtype=np.int32)
-    plan = B.mla_decode_plan(lens, 64, 128, 1)
+    plan = B.mla_decode_plan(lens, 64, 128, 1, num_sms=152)
     assert plan.workspace_bytes > B.MLA_NOALLOC_SCRATCH_BYTES
     q = torch.zeros((256, 128, 512), dtype=torch.bfloat16, device="cuda")
     qp = torch.zeros((256, 128, 64), dtype=torch.bfloat16, device="cuda")
