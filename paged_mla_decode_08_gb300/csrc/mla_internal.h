@@ -87,6 +87,7 @@ struct mla_plan {
   int max_pages = 0;  // ceil(max seq_len / page_size)
   int num_slots = 0;
   size_t ws_bytes = 0, ws_lse_offset = 0;
+  int64_t plan_capacity = 0;  // per-worker cost bound the schedule was made with
   std::vector<int32_t> seq_lens;
   std::vector<int32_t> seg_worker;  // worker of each segment (inspection)
   std::vector<mla::Segment> segs;

@@ -8,20 +8,20 @@
 // Rule.  Cut every request into 64-token tiles, n_b = ceil(L_b / 64).  There
 // are W workers (one per CTA pair, W = num_sms / 2, at most 128).  Each
 // segment (a run of tiles of one request on one worker) costs its tiles plus
-// OVH = 2 tiles of fixed work (query load, epilogue).  With S segments,
-//     total = sum_b n_b + OVH * S,   bound(w) = ceil((w + 1) * total / W),
-// worker w is filled until the cumulative cost of everything poured so far
-// reaches bound(w).  Requests are walked in order: a request that fits into
-// the worker's remaining room goes there whole; otherwise the worker takes
-// `room` tiles of it (a worker whose room is below MIN = 4 tiles and that
-// already holds work is closed first), and if that would leave fewer than MIN
-// tiles behind it takes `left - MIN` instead (or everything when that is
-// below MIN).  Because the bounds are absolute, rounding never accumulates.
-// The last worker takes whatever is left.  S is not known before pouring:
-// the first pass assumes S = B + W - 1, the second uses the first pass's S.  Zero-length requests get
-// one empty segment (it writes out = 0, lse = -inf).  A request cut into
-// k >= 2 segments gets k consecutive partial slots; a single-segment request
-// is written directly.
+// OVH = 2 tiles of fixed work (query load, epilogue).  For a capacity C,
+// fill(C) walks the requests in order and pours them into workers 0, 1, ...:
+// a request that fits the worker's room (C - cost so far - OVH) goes there
+// whole; otherwise, when room >= MIN (= 4) and at least 2 MIN tiles are left,
+// the worker takes min(room, left - MIN) tiles (no piece, the rest included,
+// is shorter than MIN); otherwise a worker that already holds work is closed,
+// and an empty one takes MIN tiles (all of them when fewer than 2 MIN are
+// left).  The last worker takes whatever is left.  C is the smallest capacity
+// (binary search upward from ceil((sum_b n_b + OVH B) / W)) whose fill keeps
+// the last worker within C, so the most loaded worker carries about the mean
+// cost; the schedule is fill(C).  A zero-length request gets one empty
+// segment (it writes out = 0, lse = -inf), placed on the next worker when it
+// does not fit.  A request cut into k >= 2 segments gets k consecutive
+// partial slots; a single-segment request is written directly.
 #include <algorithm>
 #include <cstdint>
 
@@ -58,51 +58,70 @@ int build_plan(const int32_t* seq_lens, int batch, int page_size, int num_heads,
   }
   p->max_pages = (int)((max_len + page_size - 1) / page_size);
   int64_t tiles_sum = total - (int64_t)kSegOverheadTiles * batch;
-  int64_t nsegs = (int64_t)batch + W - 1;
-  for (int pass = 0; pass < 2; ++pass) {
-  total = tiles_sum + (int64_t)kSegOverheadTiles * nsegs;
-  auto bound = [&](int w) -> int64_t { return ((int64_t)(w + 1) * total + W - 1) / W; };
+  (void)tiles_sum;
 
-  p->segs.clear(); p->seg_worker.clear();
-  int w = 0;
-  bool w_used = false;
-  int64_t cum = 0;
-  auto advance = [&]() {
-    while (w < W - 1 && cum >= bound(w)) { ++w; w_used = false; }
-  };
-  for (int b = 0; b < batch; ++b) {
-    if (tiles[b] == 0) {
-      p->segs.push_back(Segment{b, 0, 0, -1});
-      p->seg_worker.push_back(w);
-      w_used = true;
-      cum += kSegOverheadTiles;
-      advance();
-      continue;
-    }
-    int64_t t = 0;
-    while (t < tiles[b]) {
-      const int64_t left = tiles[b] - t;
-      const int64_t room = bound(w) - cum - kSegOverheadTiles;
-      int64_t n;
-      if (w == W - 1 || left <= room) {
-        n = left;
-      } else if (room < kMinSplitTiles) {
-        if (w_used) { ++w; w_used = false; continue; }
-        n = std::min<int64_t>(left, kMinSplitTiles);
-      } else {
-        n = room;
-        if (left - n < kMinSplitTiles) n = (left - kMinSplitTiles >= kMinSplitTiles) ? left - kMinSplitTiles : left;
+  // Capacity-bounded greedy fill: workers take requests in order, each up to
+  // a cost of `cap` (tiles + kSegOverheadTiles per segment); a request that
+  // does not fit is cut at the capacity, with no piece shorter than
+  // kMinSplitTiles (a worker that cannot take such a piece moves on; only a
+  // worker still empty may overshoot, by less than kMinSplitTiles).  The last
+  // worker takes whatever is left.  Returns the last worker's cost.
+  auto fill = [&](int64_t cap, bool emit) -> int64_t {
+    if (emit) { p->segs.clear(); p->seg_worker.clear(); }
+    int w = 0;
+    bool used = false;
+    int64_t cum = 0;
+    auto next_worker = [&]() { ++w; cum = 0; used = false; };
+    for (int b = 0; b < batch; ++b) {
+      if (tiles[b] == 0) {
+        if (used && w < W - 1 && cum + kSegOverheadTiles > cap) next_worker();
+        if (emit) { p->segs.push_back(Segment{b, 0, 0, -1}); p->seg_worker.push_back(w); }
+        used = true;
+        cum += kSegOverheadTiles;
+        continue;
       }
-      p->segs.push_back(Segment{b, (int32_t)t, (int32_t)(t + n), -1});
-      p->seg_worker.push_back(w);
-      w_used = true;
-      cum += n + kSegOverheadTiles;
-      t += n;
-      advance();
+      int64_t t = 0;
+      while (t < tiles[b]) {
+        const int64_t left = tiles[b] - t;
+        const int64_t room = cap - cum - kSegOverheadTiles;
+        int64_t n;
+        if (w == W - 1 || left <= room) {
+          n = left;
+        } else if (room >= kMinSplitTiles && left - kMinSplitTiles >= kMinSplitTiles) {
+          n = std::min(room, left - kMinSplitTiles);  // the rest stays >= kMinSplitTiles
+        } else if (used) {
+          next_worker();
+          continue;
+        } else {
+          n = std::min(left, (int64_t)kMinSplitTiles);  // an empty worker takes at least a minimum piece
+          if (left - n < kMinSplitTiles) n = left;
+        }
+        if (emit) {
+          p->segs.push_back(Segment{b, (int32_t)t, (int32_t)(t + n), -1});
+          p->seg_worker.push_back(w);
+        }
+        used = true;
+        cum += n + kSegOverheadTiles;
+        t += n;
+      }
     }
+    return (w == W - 1) ? cum : 0;
+  };
+  // smallest capacity whose fill leaves the last worker within it
+  int64_t lo = 1, hi = 1;
+  {
+    int64_t sum = 0;
+    for (int b = 0; b < batch; ++b) sum += tiles[b] + kSegOverheadTiles;
+    lo = std::max<int64_t>(1, (sum + W - 1) / W);
+    hi = sum + (int64_t)kSegOverheadTiles * W + kMinSplitTiles;
   }
-  nsegs = (int64_t)p->segs.size();
+  while (lo < hi) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (fill(mid, false) <= mid) hi = mid;
+    else lo = mid + 1;
   }
+  fill(lo, true);
+  p->plan_capacity = lo;
 
   // split counts and partial slots
   std::vector<int> nseg(batch, 0);

@@ -83,7 +83,9 @@ constexpr int kSlotBytes = 128 * 32 * 4;
 constexpr int OFF_RED = OFF_XCHG + kSlots * kSlotBytes;  // row max / row sum exchange, 4 KB
 constexpr int OFF_SINK = OFF_RED + 4 * 2 * 128 * 4;      // per slot 128 words: the peer's "read done" notes
 constexpr int kNoteBytes = 128 * 4;
-constexpr int OFF_BAR = OFF_SINK + kSlots * kNoteBytes;
+constexpr int OFF_SEGLEN = OFF_SINK + kSlots * kNoteBytes;  // key counts of the worker's first segments
+constexpr int kSegLenCache = 64;
+constexpr int OFF_BAR = OFF_SEGLEN + kSegLenCache * 4;
 enum Bar : int {
   B_KV_FULL = 0, B_KV_EMPTY = B_KV_FULL + kStages, B_S_FULL = B_KV_EMPTY + kStages, B_P_FULL = B_S_FULL + 2,
   B_PV_DONE, B_Q_READY, B_X_FULL, B_X_EMPTY = B_X_FULL + kSlots, B_TAIL = B_X_EMPTY + kSlots, B_FINAL,
@@ -117,6 +119,8 @@ struct Ctx {
   uint8_t* smem;     // 1024-aligned base
   uint32_t sbase;    // its shared-window address
   volatile int* abort_flag;
+  const int* seg_len;  // request_len() of segments seg0 .. seg0 + kSegLenCache - 1
+  int seg0;
   __device__ uint32_t bar(int i) const { return sbase + OFF_BAR + 8 * i; }
 };
 
@@ -153,6 +157,15 @@ __device__ __forceinline__ int request_len(const DecodeArgs& a, int b) {
   return L < cap ? L : cap;
 }
 
+// request_len() of schedule segment s, from the copy every CTA takes at start
+// (one memory round trip for all its segments instead of one per segment
+// switch in every role)
+template <int CAP>
+__device__ __forceinline__ int seg_len(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, int s) {
+  const int k = s - c.seg0;
+  return k < kSegLenCache ? c.seg_len[k] : request_len(a, sched.seg[s].req);
+}
+
 __device__ __forceinline__ int segment_tiles(const Segment& sg, int L) {
   const int last = (L + kTileTokens - 1) / kTileTokens;
   const int e = sg.tile_end < last ? sg.tile_end : last;
@@ -171,7 +184,7 @@ __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeA
   bool ok = true;
   for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
     const Segment sg = sched.seg[s];
-    const int L = request_len(a, sg.req);
+    const int L = seg_len(c, sched, a, s);
     const int nt = segment_tiles(sg, L);
     const int32_t* bt = a.block_table + (size_t)sg.req * a.bt_stride;
     if (nt > 0 && lane == 0) {
@@ -285,7 +298,7 @@ __device__ void converter(const Ctx& c, const Schedule<CAP>& sched, const Decode
   bool ok = true;
   for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
     const Segment sg = sched.seg[s];
-    const int L = request_len(a, sg.req);
+    const int L = seg_len(c, sched, a, s);
     const int nt = segment_tiles(sg, L);
     for (int jj = 0; jj < nt; ++jj, ++j) {
       const int fs = j % kStages, os = j % kF8OpStages;
@@ -356,12 +369,12 @@ __device__ void mma_issuer(const Ctx& c, const Schedule<CAP>& sched, const Decod
   // ready is issued, so S of tile j+2 never waits for P.V of tile j.
   const int seg_end = sched.worker_seg[worker + 1];
   auto first_live = [&](int s) {
-    while (s < seg_end && segment_tiles(sched.seg[s], request_len(a, sched.seg[s].req)) == 0) ++s;
+    while (s < seg_end && segment_tiles(sched.seg[s], seg_len(c, sched, a, s)) == 0) ++s;
     return s;
   };
   int s_seg = first_live(sched.worker_seg[worker]), s_jj = 0, s_j = 0, q_used = 0;
   int p_seg = s_seg, p_jj = 0, p_j = 0;
-  int s_nt = s_seg < seg_end ? segment_tiles(sched.seg[s_seg], request_len(a, sched.seg[s_seg].req)) : 0;
+  int s_nt = s_seg < seg_end ? segment_tiles(sched.seg[s_seg], seg_len(c, sched, a, s_seg)) : 0;
   int p_nt = s_nt;
   long long t_last = clock64();
   while (p_seg < seg_end) {
@@ -393,7 +406,7 @@ __device__ void mma_issuer(const Ctx& c, const Schedule<CAP>& sched, const Decod
         if (++s_jj == s_nt) {
           s_jj = 0;
           s_seg = first_live(s_seg + 1);
-          s_nt = s_seg < seg_end ? segment_tiles(sched.seg[s_seg], request_len(a, sched.seg[s_seg].req)) : 0;
+          s_nt = s_seg < seg_end ? segment_tiles(sched.seg[s_seg], seg_len(c, sched, a, s_seg)) : 0;
         }
         progressed = true;
       }
@@ -417,7 +430,7 @@ __device__ void mma_issuer(const Ctx& c, const Schedule<CAP>& sched, const Decod
       if (++p_jj == p_nt) {
         p_jj = 0;
         p_seg = first_live(p_seg + 1);
-        p_nt = p_seg < seg_end ? segment_tiles(sched.seg[p_seg], request_len(a, sched.seg[p_seg].req)) : 0;
+        p_nt = p_seg < seg_end ? segment_tiles(sched.seg[p_seg], seg_len(c, sched, a, p_seg)) : 0;
       }
       progressed = true;
     }
@@ -477,7 +490,7 @@ __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const Decode
   bool ok = true;
   for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
     const Segment sg = sched.seg[s];
-    const int nt = segment_tiles(sg, request_len(a, sg.req));
+    const int nt = segment_tiles(sg, seg_len(c, sched, a, s));
     if (nt == 0) continue;
     // ---- this segment's query: latent half -> TMEM columns [384, 512), rope
     // half -> shared memory (64B swizzle).  The previous segment's S MMAs all
@@ -616,7 +629,7 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
   for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
     const Segment sg = sched.seg[s];
     const int b = sg.req;
-    const int L = request_len(a, b);
+    const int L = seg_len(c, sched, a, s);
     const int nt = segment_tiles(sg, L);
     const int vis = valid_row ? L - a.q_len + 1 + qi : 0;  // visible keys of this row
     float m_ref = -CUDART_INF_F, l = 0.f;
@@ -817,6 +830,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int rank = (int)cluster_ctarank();
   const int worker = blockIdx.x >> 1;
+  c.seg_len = reinterpret_cast<const int*>(c.smem + OFF_SEGLEN);
+  c.seg0 = worker < sched.num_workers ? sched.worker_seg[worker] : 0;
+  if (warp == 2 && worker < sched.num_workers) {
+    // key counts of this worker's segments, read once for every role
+    const int n = min(sched.worker_seg[worker + 1] - c.seg0, kSegLenCache);
+    for (int i = threadIdx.x & 31; i < n; i += 32)
+      reinterpret_cast<int*>(c.smem + OFF_SEGLEN)[i] = request_len(a, sched.seg[c.seg0 + i].req);
+  }
 
   if (threadIdx.x == 0) {
     *c.abort_flag = 0;

@@ -13,51 +13,55 @@ from paged_mla_decode_08_gb300 import workloads as W
 
 
 def plan_rule(lens, workers, tile, ovh, min_split):
-    """The planner's rule, restated: worker w is filled until the cumulative
-    cost (tiles + ovh per segment) reaches ceil((w+1) * total / W); two
-    passes, the second sized with the first pass's segment count."""
+    """The planner's rule, restated: a capacity-bounded greedy fill of the
+    workers in request order (tiles + ovh per segment, pieces of at least
+    min_split tiles), at the smallest capacity whose fill keeps the last
+    worker within it."""
     tiles = [-(-int(L) // tile) for L in lens]
-    nsegs = len(lens) + workers - 1
-    for _ in range(2):
-        total = sum(tiles) + ovh * nsegs
-        bound = lambda w: -(-(w + 1) * total // workers)  # noqa: E731
+    W = workers
+
+    def fill(cap, emit):
         segs = []
         w, used, cum = 0, False, 0
-
-        def advance():
-            nonlocal w, used
-            while w < workers - 1 and cum >= bound(w):
-                w, used = w + 1, False
-
         for b, n_b in enumerate(tiles):
             if n_b == 0:
+                if used and w < W - 1 and cum + ovh > cap:
+                    w, used, cum = w + 1, False, 0
                 segs.append([w, b, 0, 0])
                 used = True
                 cum += ovh
-                advance()
                 continue
             t = 0
             while t < n_b:
                 left = n_b - t
-                room = bound(w) - cum - ovh
-                if w == workers - 1 or left <= room:
+                room = cap - cum - ovh
+                if w == W - 1 or left <= room:
                     n = left
-                elif room < min_split:
-                    if used:
-                        w, used = w + 1, False
-                        continue
-                    n = min(left, min_split)
+                elif room >= min_split and left - min_split >= min_split:
+                    n = min(room, left - min_split)
+                elif used:
+                    w, used, cum = w + 1, False, 0
+                    continue
                 else:
-                    n = room
+                    n = min(left, min_split)
                     if left - n < min_split:
-                        n = left - min_split if left - min_split >= min_split else left
+                        n = left
                 segs.append([w, b, t, t + n])
                 used = True
                 cum += n + ovh
                 t += n
-                advance()
-        nsegs = len(segs)
-    cap = -(-total // workers)
+        return segs, (cum if w == W - 1 else 0)
+
+    total = sum(n + ovh for n in tiles)
+    lo, hi = max(1, -(-total // W)), total + ovh * W + min_split
+    while lo < hi:
+        mid = (lo + hi) // 2
+        if fill(mid, False)[1] <= mid:
+            hi = mid
+        else:
+            lo = mid + 1
+    segs, _ = fill(lo, True)
+    cap = lo
     counts = {}
     for s in segs:
         counts[s[1]] = counts.get(s[1], 0) + 1
@@ -126,12 +130,14 @@ def test_plan_matches_rule(name, sms):
     else:
         want_ws = 0
     assert p.workspace_bytes == want_ws
-    # balance: every worker (the last included) ends within one minimum piece
-    # plus one segment overhead (plus a stub) of its share
+    # balance: no worker exceeds the capacity (an empty worker's minimum
+    # piece aside), and the capacity is within a couple of pieces of the mean
     loads = np.zeros(sms // 2, dtype=np.int64)
     for w_, b, t0, t1, _ in segs:
         loads[w_] += (t1 - t0) + ovh
-    assert loads.max(initial=0) <= cap + 2 * mn + 2 * ovh, (loads.max(), cap)
+    assert loads.max(initial=0) <= cap + mn, (loads.max(), cap)
+    mean = -(-sum(-(-int(L) // tile) + ovh for L in lens) // (sms // 2))
+    assert cap <= mean + 2 * (mn + ovh) or len(lens) < sms // 2, (cap, mean)
 
 
 def test_plan_fuzz():
