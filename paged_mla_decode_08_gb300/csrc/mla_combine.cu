@@ -40,6 +40,11 @@ template <int CAP>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineList<CAP> jobs,
                                                       const __grid_constant__ DecodeArgs a) {
   extern __shared__ float s_w[];  // [nsplit][32] weights (0 for -inf splits)
+  // Launched as a programmatic dependent of the main kernel: everything above
+  // this wait overlaps the main kernel's tail; the partials are read after it
+  // (the wait returns once the main grid has completed and its writes are
+  // visible; without the launch attribute it returns at once).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const CombineJob job = jobs.job[blockIdx.x];
   const int M = a.rows;
   const int r0 = blockIdx.y * kCombRows;
@@ -141,10 +146,20 @@ static cudaError_t launch_combine_cap(const std::vector<CombineJob>& jobs, const
   int maxsplit = 1;
   for (const CombineJob& j : jobs) maxsplit = j.nsplit > maxsplit ? j.nsplit : maxsplit;
   const size_t smem = (size_t)maxsplit * kCombRows * sizeof(float);  // <= 128 splits: 16 KB
-  combine_kernel<CAP><<<dim3((unsigned)jobs.size(), (unsigned)((a.rows + kCombRows - 1) / kCombRows),
-                             (unsigned)(kChunks / kCombChunks)),
-                        256, smem, stream>>>(list, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)jobs.size(), (unsigned)((a.rows + kCombRows - 1) / kCombRows),
+                     (unsigned)(kChunks / kCombChunks));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  // programmatic dependent launch: the grid may start while the main kernel
+  // (the previous launch on the stream) finishes; see griddepcontrol.wait
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel<CAP>, list, a);
 }
 
 cudaError_t launch_combine(const std::vector<CombineJob>& jobs, const DecodeArgs& a,

@@ -896,6 +896,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // every global write of this CTA is issued: a programmatic dependent
+  // (the combine) may be scheduled once all CTAs got here; it still waits
+  // for this grid's completion before it reads anything
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
   cluster_sync();  // no peer may still write into this CTA's shared memory
 }
