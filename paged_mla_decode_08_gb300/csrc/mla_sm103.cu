@@ -56,20 +56,23 @@ namespace sm103 {
 using namespace mla::ptx;
 
 constexpr int kThreads = 512;  // warps 0-3: producer, MMA, 2 converter (e4m3); 4-11: softmax; 12-15: exchange
-constexpr int kStages = 4;  // bf16 cache: operand stages; e4m3 cache: fp8 staging stages
+constexpr int kStages = 4;  // cache-tile ring stages (bf16); the e4m3 split of the same bytes is below
 constexpr int kLatBox = 64 * 128;           // 64 tokens x 64 bf16 columns, 128B swizzle
 constexpr int kRopeBox = 64 * 64;           // 64 tokens x 32 bf16 columns, 64B swizzle
 constexpr int kStageBytes = 4 * kLatBox + kRopeBox;  // 36864
 constexpr int kStageTx = kStageBytes;       // bytes TMA delivers per tile
 constexpr int OFF_KV = 0;
-// e4m3 cache: the first 144 KB hold 2 fp16 operand stages (same layout as a
-// bf16 stage) followed by 4 fp8 staging stages, each 64 keys x (256 latent +
-// 32 rope) bytes, unswizzled.
-constexpr int kF8OpStages = 2;
+// e4m3 cache: the first 144 KB hold kF8OpStages fp16 operand stages (same
+// layout as a bf16 stage) followed by kF8Stages fp8 staging stages, each 64
+// keys x (256 latent + 32 rope) bytes, unswizzled.  An operand stage is held
+// from conversion until its P.V completes, so operand stages are the scarce
+// ones; a raw tile is held only from its load until converted.
+constexpr int kF8OpStages = 3;
+constexpr int kF8Stages = 2;
 constexpr int kF8StageBytes = 64 * 288;
 constexpr int kF8RopeOff = 64 * 256;
 constexpr int OFF_F8 = kF8OpStages * kStageBytes;
-static_assert(OFF_F8 + kStages * kF8StageBytes == kStages * kStageBytes, "fp8 ring fits the operand ring");
+static_assert(OFF_F8 + kF8Stages * kF8StageBytes <= kStages * kStageBytes, "fp8 ring fits the operand ring");
 template <bool F8>
 __host__ __device__ constexpr int op_stages() { return F8 ? kF8OpStages : kStages; }
 constexpr int OFF_QROPE = kStages * kStageBytes;       // 128 rows x 64 B
@@ -197,10 +200,10 @@ __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeA
                        (uint32_t)a.rows * kRope * 2);
     }
     for (int jj = 0; jj < nt; ++jj, ++j) {
-      const int stage = j % kStages;
+      const int stage = j % (F8 ? kF8Stages : kStages);
       if (F8) {
         // raw e4m3 tile into the fp8 ring; the converter warps expand it
-        if (j >= kStages && !wait_bar_warp<false>(c, c.bar(B_F8_EMPTY + stage), ((j / kStages) - 1) & 1, 0x103)) {
+        if (j >= kF8Stages && !wait_bar_warp<false>(c, c.bar(B_F8_EMPTY + stage), ((j / kF8Stages) - 1) & 1, 0x103)) {
           ok = false;
           break;
         }
@@ -274,9 +277,10 @@ __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeA
   // drain: the copies of the last stages must have landed before the CTA leaves
   const int issued = j;
   const int landed_bar = F8 ? B_F8_FULL : B_KV_FULL;
-  for (int k = issued - 1; k >= 0 && k >= issued - kStages; --k) {
+  constexpr int ring = F8 ? kF8Stages : kStages;
+  for (int k = issued - 1; k >= 0 && k >= issued - ring; --k) {
     const long long t0 = clock64();
-    while (!mbar_try_wait(c.bar(landed_bar + (k % kStages)), (k / kStages) & 1) && clock64() - t0 < kTimeoutCycles) {
+    while (!mbar_try_wait(c.bar(landed_bar + (k % ring)), (k / ring) & 1) && clock64() - t0 < kTimeoutCycles) {
     }
   }
 }
@@ -301,8 +305,8 @@ __device__ void converter(const Ctx& c, const Schedule<CAP>& sched, const Decode
     const int L = seg_len(c, sched, a, s);
     const int nt = segment_tiles(sg, L);
     for (int jj = 0; jj < nt; ++jj, ++j) {
-      const int fs = j % kStages, os = j % kF8OpStages;
-      if (!wait_bar_warp<false>(c, c.bar(B_F8_FULL + fs), (j / kStages) & 1, 0x501)) { ok = false; break; }
+      const int fs = j % kF8Stages, os = j % kF8OpStages;
+      if (!wait_bar_warp<false>(c, c.bar(B_F8_FULL + fs), (j / kF8Stages) & 1, 0x501)) { ok = false; break; }
       if (j >= kF8OpStages &&
           !wait_bar_warp<false>(c, c.bar(B_KV_EMPTY + os), ((j / kF8OpStages) - 1) & 1, 0x502)) {
         ok = false;
