@@ -190,6 +190,25 @@ __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeA
     const int L = seg_len(c, sched, a, s);
     const int nt = segment_tiles(sg, L);
     const int32_t* bt = a.block_table + (size_t)sg.req * a.bt_stride;
+    // block-table entries of the segment's pages, 32 per load (one per
+    // lane), the next 32 requested while the current ones are used: page
+    // lookups add no memory latency per tile.  Entries past the request's
+    // length are read (inside the row) but never used.
+    const int pg_begin = sg.tile_begin * pieces;
+    const int pg_end = min(sg.tile_end * pieces, a.bt_stride);
+    auto load_chunk = [&](int ch) {
+      const int q = pg_begin + (ch << 5) + lane;
+      return q < pg_end ? __ldg(bt + q) : -1;
+    };
+    int chunk = 0, pid_cur = load_chunk(0), pid_next = load_chunk(1);
+    auto page_id = [&](int pg) {  // warp-uniform pg >= the previous one
+      const int ch = (pg - pg_begin) >> 5;
+      while (chunk < ch) {
+        pid_cur = pid_next;
+        pid_next = load_chunk(++chunk + 1);
+      }
+      return __shfl_sync(0xffffffffu, pid_cur, (pg - pg_begin) & 31);
+    };
     if (nt > 0 && lane == 0) {
       // the exchange warps load this request's query when the segment
       // starts: pull it into L2 now, a few tiles ahead (the M rows are
@@ -207,16 +226,18 @@ __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeA
           ok = false;
           break;
         }
+        const int tok0 = (sg.tile_begin + jj) * kTileTokens;
+        const int pid0 = page_id((sg.tile_begin + jj) * pieces);
+        const int pid1 = pieces > 1 ? page_id((sg.tile_begin + jj) * pieces + 1) : -1;
         if (lane == 0) {
           const uint32_t full = c.bar(B_F8_FULL + stage);
           const uint32_t dst = c.sbase + OFF_F8 + stage * kF8StageBytes;
-          const int tok0 = (sg.tile_begin + jj) * kTileTokens;
           mbar_arrive_expect_tx(full, kF8StageBytes);
           for (int pc = 0; pc < pieces; ++pc) {
             const int ptok = tok0 + pc * a.page_size;
             int y = oob_row;
             if (ptok < L) {
-              const int pid = bt[ptok / a.page_size];
+              const int pid = pc ? pid1 : pid0;
               if (pid >= 0 && pid < a.num_pages) y = pid * a.page_size;
             }
             const uint32_t rows = pc * a.page_size;
@@ -237,13 +258,15 @@ __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeA
       const uint32_t full = c.bar(B_KV_FULL + stage);
       const uint32_t land = tail ? c.bar(B_TAIL) : full;
       const uint32_t dst = c.sbase + OFF_KV + stage * kStageBytes;
+      const int pid0 = page_id(t * pieces);
+      const int pid1 = pieces > 1 ? page_id(t * pieces + 1) : -1;
       if (lane == 0) {
         mbar_arrive_expect_tx(land, kStageTx);
         for (int pc = 0; pc < pieces; ++pc) {
           const int ptok = tok0 + pc * a.page_size;
           int y = oob_row;
           if (ptok < L) {
-            const int pid = bt[ptok / a.page_size];
+            const int pid = pc ? pid1 : pid0;
             if (pid >= 0 && pid < a.num_pages) y = pid * a.page_size;
           }
           const uint32_t rows = pc * a.page_size;

@@ -184,3 +184,32 @@ def test_side_stream():
         R.decode(db)
     s.synchronize()
     check(w, db.out, db.lse, *oracle(w))
+
+
+def test_cuda_graph_replay_with_new_lengths():
+    """Graph-captured decode: planned once from upper-bound lengths, captured
+    (main kernel + combine, with its programmatic-dependent edge) into a CUDA
+    graph, then replayed after the device lengths change; each replay must
+    match the oracle for the lengths it ran with."""
+    lens = np.array([2000, 1000, 300, 5, 64, 1500], dtype=np.int32)
+    upper = np.array([2600, 1600, 900, 700, 700, 2100], dtype=np.int32)
+    w = W.make_workload("dsv3", seed=14, seq_lens=list(lens), bt_extra_cols=12)
+    db = R.upload(w, plan_seq_lens=upper)
+    R.decode(db)  # warm: one-time host work (tensor-map encoder lookup) outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            B.mla_decode(db.plan, db.q_nope, db.q_pe, db.kv, db.kv_dtype, db.block_table, db.seq_lens,
+                         w.scale, w.k_scale, db.out, db.lse, db.workspace, None, s)
+    for new_lens in (lens, np.array([1999, 63, 1, 0, 64, 2100], dtype=np.int32)):
+        db.seq_lens.copy_(torch.from_numpy(new_lens))
+        db.out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert B.mla_decode_device_error() == 0
+        ref_out, ref_lse = O.mla_decode(w.q_nope_bits, w.q_pe_bits, w.kv_bits, w.kv_dtype, w.block_table,
+                                        new_lens, w.q_len, w.page_size, w.scale, w.k_scale)
+        check(w, db.out, db.lse, ref_out, ref_lse)
