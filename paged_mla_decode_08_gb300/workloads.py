@@ -279,3 +279,56 @@ def workload_stats(w: Workload) -> dict:
         alg_bytes=kv_bytes + q_bytes + out_bytes + lse_bytes + bt_bytes,
         flops=flops, tokens=t,
     )
+
+
+# ---------------------------------------------------------------- request pools
+
+
+@dataclass
+class RequestPool:
+    """A serving-side request pool holding the pages of a batch.
+
+    ``req_to_token [pool_rows, token_cols]`` int32: cache slot of each token
+    of a pool row, slot = page id * page_size + offset in the page (the cache
+    is ``[num_pages, page_size, 576]``, one slot per row); slots of tokens a
+    request does not have are ``unused_slot``.  ``req_to_page [pool_rows,
+    page_cols]`` int32: the same pages as a page list, 0 past a request's
+    pages.  ``req_pool_indices [batch]`` int32: the pool row of each request
+    of the batch.  Rows no request of the batch owns hold random values.
+    """
+
+    req_to_token: np.ndarray
+    req_to_page: np.ndarray
+    req_pool_indices: np.ndarray
+    page_size: int
+
+
+def make_request_pool(block_table: np.ndarray, seq_lens: np.ndarray, page_size: int, pool_rows: int,
+                      seed: int = 0, token_cols: int | None = None, page_cols: int | None = None,
+                      unused_slot: int = 2 ** 31 - 1) -> RequestPool:
+    """Lay the pages of ``block_table`` (first ceil(L/page) entries of each
+    row) into a request pool whose rows are a seeded random choice of
+    ``pool_rows`` rows."""
+    rng = np.random.default_rng(seed)
+    batch = len(seq_lens)
+    assert pool_rows >= batch
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    pages = (lens + page_size - 1) // page_size
+    need_pages = int(pages.max(initial=0))
+    if page_cols is None:
+        page_cols = max(need_pages, 1)
+    if token_cols is None:
+        token_cols = page_cols * page_size
+    assert page_cols >= need_pages and token_cols >= need_pages * page_size
+    rows = rng.choice(pool_rows, size=batch, replace=False).astype(np.int32)
+    r2t = rng.integers(0, 2 ** 31 - 1, size=(pool_rows, token_cols), dtype=np.int64).astype(np.int32)
+    r2p = rng.integers(0, 2 ** 31 - 1, size=(pool_rows, page_cols), dtype=np.int64).astype(np.int32)
+    for b in range(batch):
+        r = rows[b]
+        n = int(pages[b])
+        r2t[r, :] = unused_slot
+        r2p[r, :] = 0
+        r2p[r, :n] = block_table[b, :n]
+        j = np.arange(int(lens[b]), dtype=np.int64)
+        r2t[r, : len(j)] = (block_table[b, j // page_size].astype(np.int64) * page_size + j % page_size).astype(np.int32)
+    return RequestPool(req_to_token=r2t, req_to_page=r2p, req_pool_indices=rows, page_size=page_size)
