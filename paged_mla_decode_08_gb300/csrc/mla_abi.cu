@@ -145,7 +145,7 @@ int mla_decode_plan(const int32_t* seq_lens_host, int batch, int page_size, int 
   const char* msg = "";
   int rc = mla::build_plan(seq_lens_host, batch, page_size, num_heads, q_len, num_sms, p, &msg);
   if (rc != MLA_OK) { delete p; return fail(rc, msg); }
-  if (p->segs.size() > (size_t)mla::kSegCapLarge || p->jobs.size() > (size_t)mla::kJobCapLarge) {
+  if (p->segs.size() > (size_t)mla::kSegCapLarge || p->jobs.size() > (size_t)mla::kJobCap) {
     delete p;
     return fail(MLA_ERR_ARG, "batch too large: the schedule exceeds one launch's segment capacity");
   }

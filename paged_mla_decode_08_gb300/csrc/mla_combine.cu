@@ -165,8 +165,7 @@ static cudaError_t launch_combine_cap(const std::vector<CombineJob>& jobs, const
 cudaError_t launch_combine(const std::vector<CombineJob>& jobs, const DecodeArgs& a,
                            cudaStream_t stream) {
   if (jobs.empty()) return cudaSuccess;
-  if (jobs.size() <= (size_t)kJobCapSmall) return launch_combine_cap<kJobCapSmall>(jobs, a, stream);
-  return launch_combine_cap<kJobCapLarge>(jobs, a, stream);
+  return launch_combine_cap<kJobCap>(jobs, a, stream);
 }
 
 }  // namespace mla

@@ -52,8 +52,10 @@ struct CombineList {
   int32_t pad[3];
   CombineJob job[CAP];
 };
-constexpr int kJobCapSmall = 448;
-constexpr int kJobCapLarge = 1984;
+// Every split request spans at least one worker boundary, so a plan has at
+// most kMaxWorkers - 1 combine jobs; one capacity covers all plans.
+constexpr int kJobCap = 128;
+static_assert(kJobCap >= kMaxWorkers - 1, "combine job capacity");
 
 // Pointers and scalars of one decode call, as the kernels see them.
 struct DecodeArgs {

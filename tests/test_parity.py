@@ -213,3 +213,13 @@ def test_cuda_graph_replay_with_new_lengths():
         ref_out, ref_lse = O.mla_decode(w.q_nope_bits, w.q_pe_bits, w.kv_bits, w.kv_dtype, w.block_table,
                                         new_lens, w.q_len, w.page_size, w.scale, w.k_scale)
         check(w, db.out, db.lse, ref_out, ref_lse)
+
+
+def test_wide_batch_large_schedule():
+    """700 short requests: more segments than the small schedule capacity,
+    so the launch takes the large-capacity kernel instantiation."""
+    lens = np.random.default_rng(15).integers(0, 200, size=700)
+    w = W.make_workload("tiny", seed=15, seq_lens=list(lens), num_heads=16, pool_pages=4096)
+    db, out, lse = run_gpu(w)
+    assert len(db.plan.segments()) > 448
+    check(w, out, lse, *oracle(w))
