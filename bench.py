@@ -301,6 +301,8 @@ def our_arm(args, w, rank, world):
 
     # ---- e2e: host buffers in, results back to the host, copies timed
     e2e = e2e_measure(db, w, dev, stream, max(3, min(K, 200)))
+    # ---- the step before the decode: block-table construction, timed alone
+    bt_rows = block_table_measure(w, dev, stream, flush, max(3, min(K, 200)))
 
     if rank != 0:
         return
@@ -342,10 +344,55 @@ def our_arm(args, w, rank, world):
         "main_ms_median": statistics.median(main_ms),
         "t_roof_us": {"hbm": t_hbm * 1e6, "tensor": t_tc * 1e6},
         "wall_s_timed_loop": wall,
+        "block_table_build": bt_rows,
         "segments": int(len(db.plan.segments())), "partial_slots": db.plan.num_partial_slots,
         "kernel_source_sha": kernel_source_hash(),
     }
     print(json.dumps(line), flush=True)
+
+
+def block_table_measure(w, dev, stream, flush, K):
+    """Both block-table builders over a request pool holding this workload's
+    pages (pool rows = batch + 64), each launch timed with events after an L2
+    flush.  Algorithmic bytes: one int32 pool read per live table entry plus
+    the row index (and, for the token pool, the length) per request, and the
+    whole int32 table written."""
+    import torch
+    from paged_mla_decode_08_gb300 import binding as B
+    pool = W.make_request_pool(w.block_table, w.seq_lens, w.page_size, pool_rows=w.batch + 64, seed=1)
+    r2t = torch.from_numpy(pool.req_to_token).to(dev)
+    r2p = torch.from_numpy(pool.req_to_page).to(dev)
+    idx = torch.from_numpy(pool.req_pool_indices).to(dev)
+    lens = torch.from_numpy(np.ascontiguousarray(w.seq_lens)).to(dev)
+    max_blocks = int(w.block_table.shape[1])
+    bt = torch.empty((w.batch, max_blocks), dtype=torch.int32, device=dev)
+    live = int(((w.seq_lens.astype(np.int64) + w.page_size - 1) // w.page_size).sum())
+    table_bytes = w.batch * max_blocks * 4
+    calls = {
+        "from_tokens": (lambda: B.mla_block_table_from_tokens(r2t, idx, lens, w.page_size, bt, stream),
+                        live * 4 + w.batch * 8 + table_bytes),
+        "from_pages": (lambda: B.mla_block_table_from_pages(r2p, idx, bt, stream),
+                       w.batch * min(max_blocks, r2p.shape[1]) * 4 + w.batch * 4 + table_bytes),
+    }
+    res = {}
+    for name, (fn, alg) in calls.items():
+        for _ in range(3):
+            fn()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for k in range(K):
+            flush.zero_()
+            ev[k][0].record(stream)
+            fn()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        us = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+        res[name] = {"us": us, "alg_bytes": alg, "achieved_gbs": alg / (us * 1e-6) / 1e9,
+                     "bound": "latency", "launches": K}
+    want = np.where(np.arange(max_blocks)[None, :] < ((w.seq_lens[:, None] + w.page_size - 1) // w.page_size),
+                    w.block_table, 0)
+    got = bt.cpu().numpy()
+    res["last_table_matches_workload"] = bool(np.array_equal(got, want))
+    return res
 
 
 def e2e_measure(db, w, dev, stream, K):

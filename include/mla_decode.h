@@ -186,6 +186,60 @@ int mla_decode_noalloc(const mla_plan* plan, const void* q_nope, const void* q_p
                        const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
                        void* stream);
 
+/* ---- block-table construction (the step before the decode) ----
+ *
+ * Build the [batch, max_blocks] int32 block table mla_decode reads from a
+ * serving-side request pool, on the device and asynchronously on `stream`
+ * (no host synchronisation, so both may be captured in a CUDA graph with the
+ * decode).  The serving pages do this right before the decode: sglang
+ * trtllm_mla_backend.py, TRTLLMMLABackend._create_block_kv_indices (a token
+ * pool, create_flashmla_kv_indices_triton) and tokenspeed trtllm_mla.py,
+ * TRTLLMMLABackend._create_block_kv_indices / tokenspeed flashmla.py,
+ * _init_decode_metadata (a page pool, req_to_page[req_pool_indices]).
+ *
+ * Shared arguments:
+ *   req_pool_indices  device int32 [batch]: pool row of each request.
+ *   batch             requests, 1 .. 2^24.
+ *   block_table       device int32 [batch, max_blocks], row-major; every
+ *                     entry is written.
+ *   max_blocks        1 .. MLA_BLOCK_TABLE_MAX_BLOCKS.
+ * All int32 arrays 4-byte aligned; the caller owns every buffer.
+ *
+ * Device-side errors.  A pool row index outside [0, pool_rows), a lookup past
+ * the pool's columns, a negative length or a negative token slot is not
+ * read: the entry gets the padding value and the first such event since the
+ * last reset is recorded in the word mla_decode_device_error reports
+ * (0x301 row index, 0x302 column, 0x303 negative seq_len, 0x304 negative
+ * slot).  Host-side errors: MLA_ERR_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA.
+ */
+#define MLA_BLOCK_TABLE_MAX_BLOCKS (65535 * 256)
+
+/*
+ * From a token pool: req_to_token is device int32 [pool_rows, token_cols],
+ * row-major, the cache slot of each token of a pool row, where slot =
+ * page_id * page_size + offset in the page (the cache viewed as
+ * [num_pages, page_size, 576]).  With L = seq_lens[b] (device int32
+ * [batch]):
+ *   block_table[b][i] = req_to_token[req_pool_indices[b]][i * page_size] / page_size
+ *                                              for i < ceil(L / page_size),
+ *                     = -1                     otherwise
+ * (the page of the first token of each of the request's pages).
+ * page_size: 32 or 64.
+ */
+int mla_block_table_from_tokens(const int32_t* req_to_token, int64_t pool_rows, int64_t token_cols,
+                                const int32_t* req_pool_indices, const int32_t* seq_lens, int batch,
+                                int page_size, int32_t* block_table, int max_blocks, void* stream);
+
+/*
+ * From a page pool: req_to_page is device int32 [pool_rows, page_cols],
+ * row-major, the page ids of each pool row.
+ *   block_table[b][i] = req_to_page[req_pool_indices[b]][i]   for i < min(max_blocks, page_cols),
+ *                     = 0                                     otherwise.
+ */
+int mla_block_table_from_pages(const int32_t* req_to_page, int64_t pool_rows, int64_t page_cols,
+                               const int32_t* req_pool_indices, int batch, int32_t* block_table,
+                               int max_blocks, void* stream);
+
 /* ---- plan inspection (host only; used by tests and tools) ---- */
 
 /* Device workspace bytes the plan needs. */
@@ -210,7 +264,8 @@ void mla_planner_constants(int* tile_tokens, int* segment_overhead_tiles, int* m
 
 /* Kernel-side error word of the current device: 0, or the code of the first
  * bounded wait that timed out inside a decode kernel since the last reset
- * (the kernel then stopped early and its outputs are not valid).  Reading it
+ * (the kernel then stopped early and its outputs are not valid); failing
+ * that, the first out-of-range lookup of a block-table builder (0x30x).  Reading it
  * synchronises with the device; reset != 0 clears it.  Errors: MLA_ERR_ARG,
  * MLA_ERR_CUDA. */
 int mla_decode_device_error(int* code, int reset);

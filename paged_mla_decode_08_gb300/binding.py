@@ -37,6 +37,10 @@ SIGNATURES = {
     "mla_decode_main": (_c_int, _DECODE_ARGS),
     "mla_decode_combine": (_c_int, [_vp, _vp, _vp, _vp, _c_size, _vp]),
     "mla_decode_noalloc": (_c_int, _DECODE_ARGS[:16] + [_vp]),
+    "mla_block_table_from_tokens": (_c_int, [_vp, ctypes.c_int64, ctypes.c_int64, _vp, _vp, _c_int, _c_int,
+                                             _vp, _c_int, _vp]),
+    "mla_block_table_from_pages": (_c_int, [_vp, ctypes.c_int64, ctypes.c_int64, _vp, _c_int, _vp, _c_int,
+                                            _vp]),
     "mla_plan_workspace_bytes": (_c_size, [_vp]),
     "mla_plan_num_workers": (_c_int, [_vp]),
     "mla_plan_num_segments": (_c_int, [_vp]),
@@ -185,6 +189,26 @@ def mla_decode_noalloc(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_
 
 
 MLA_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+MLA_BLOCK_TABLE_MAX_BLOCKS = 65535 * 256
+
+
+def mla_block_table_from_tokens(req_to_token, req_pool_indices, seq_lens, page_size: int, block_table,
+                                stream=None):
+    """Fill ``block_table`` (int32 CUDA [batch, max_blocks]) from a token pool
+    ``req_to_token`` (int32 CUDA [pool_rows, token_cols], contiguous)."""
+    rows, cols = req_to_token.shape
+    _check(load().mla_block_table_from_tokens(_ptr(req_to_token), int(rows), int(cols), _ptr(req_pool_indices),
+                                              _ptr(seq_lens), int(block_table.shape[0]), int(page_size),
+                                              _ptr(block_table), int(block_table.shape[1]), _stream(stream)))
+
+
+def mla_block_table_from_pages(req_to_page, req_pool_indices, block_table, stream=None):
+    """Fill ``block_table`` (int32 CUDA [batch, max_blocks]) from a page pool
+    ``req_to_page`` (int32 CUDA [pool_rows, page_cols], contiguous)."""
+    rows, cols = req_to_page.shape
+    _check(load().mla_block_table_from_pages(_ptr(req_to_page), int(rows), int(cols), _ptr(req_pool_indices),
+                                             int(block_table.shape[0]), _ptr(block_table),
+                                             int(block_table.shape[1]), _stream(stream)))
 
 
 def mla_planner_constants():

@@ -18,6 +18,14 @@ cudaError_t launch_sm103(const mla_plan& p, const DecodeArgs& a, cudaStream_t st
 cudaError_t sm103_read_error(int* code, bool reset);
 cudaError_t launch_combine(const std::vector<CombineJob>& jobs, const DecodeArgs& a,
                            cudaStream_t stream);
+cudaError_t launch_block_table_from_tokens(const int32_t* req_to_token, int64_t pool_rows,
+                                           int64_t token_cols, const int32_t* req_pool_indices,
+                                           const int32_t* seq_lens, int batch, int page_size,
+                                           int32_t* block_table, int max_blocks, cudaStream_t stream);
+cudaError_t launch_block_table_from_pages(const int32_t* req_to_page, int64_t pool_rows, int64_t page_cols,
+                                          const int32_t* req_pool_indices, int batch, int32_t* block_table,
+                                          int max_blocks, cudaStream_t stream);
+cudaError_t block_table_read_error(int* code, bool reset);
 }  // namespace mla
 
 namespace {
@@ -237,8 +245,53 @@ const char* mla_decode_last_error_string(void) { return g_last_error.c_str(); }
 
 int mla_decode_device_error(int* code, int reset) {
   if (!code) return fail(MLA_ERR_ARG, "code is NULL");
+  int bt_code = 0;
   cudaError_t e = mla::sm103_read_error(code, reset != 0);
+  if (e == cudaSuccess) e = mla::block_table_read_error(&bt_code, reset != 0);
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("reading the kernel error word: ") + cudaGetErrorString(e));
+  if (*code == 0) *code = bt_code;
+  return ok();
+}
+
+// Shared argument checks of the two block-table builders.
+static int check_block_table_args(const int32_t* pool, int64_t pool_rows, int64_t pool_cols,
+                                  const int32_t* req_pool_indices, int batch, int32_t* block_table,
+                                  int max_blocks) {
+  if (!pool || !req_pool_indices || !block_table) return fail(MLA_ERR_ARG, "a required device pointer is NULL");
+  if (batch < 1 || batch > (1 << 24)) return fail(MLA_ERR_ARG, "batch must be in [1, 2^24]");
+  if (max_blocks < 1 || max_blocks > MLA_BLOCK_TABLE_MAX_BLOCKS)
+    return fail(MLA_ERR_ARG, "max_blocks must be in [1, MLA_BLOCK_TABLE_MAX_BLOCKS]");
+  if (pool_rows < 1 || pool_cols < 1 || pool_rows > (INT64_MAX / pool_cols))
+    return fail(MLA_ERR_ARG, "pool_rows and pool columns must be >= 1");
+  if (!aligned(pool, 4) || !aligned(req_pool_indices, 4) || !aligned(block_table, 4))
+    return fail(MLA_ERR_ARG, "int32 arrays must be 4-byte aligned");
+  return check_device(nullptr);
+}
+
+int mla_block_table_from_tokens(const int32_t* req_to_token, int64_t pool_rows, int64_t token_cols,
+                                const int32_t* req_pool_indices, const int32_t* seq_lens, int batch,
+                                int page_size, int32_t* block_table, int max_blocks, void* stream) {
+  if (page_size != 32 && page_size != 64) return fail(MLA_ERR_ARG, "page_size must be 32 or 64");
+  if (!seq_lens || !aligned(seq_lens, 4)) return fail(MLA_ERR_ARG, "seq_lens must be a 4-byte aligned device pointer");
+  int rc = check_block_table_args(req_to_token, pool_rows, token_cols, req_pool_indices, batch, block_table,
+                                  max_blocks);
+  if (rc != MLA_OK) return rc;
+  cudaError_t e = mla::launch_block_table_from_tokens(req_to_token, pool_rows, token_cols, req_pool_indices,
+                                                      seq_lens, batch, page_size, block_table, max_blocks,
+                                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("block-table launch: ") + cudaGetErrorString(e));
+  return ok();
+}
+
+int mla_block_table_from_pages(const int32_t* req_to_page, int64_t pool_rows, int64_t page_cols,
+                               const int32_t* req_pool_indices, int batch, int32_t* block_table,
+                               int max_blocks, void* stream) {
+  int rc = check_block_table_args(req_to_page, pool_rows, page_cols, req_pool_indices, batch, block_table,
+                                  max_blocks);
+  if (rc != MLA_OK) return rc;
+  cudaError_t e = mla::launch_block_table_from_pages(req_to_page, pool_rows, page_cols, req_pool_indices, batch,
+                                                     block_table, max_blocks, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("block-table launch: ") + cudaGetErrorString(e));
   return ok();
 }
 

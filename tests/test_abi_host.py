@@ -89,9 +89,19 @@ def test_decode_null_plan():
     assert rc == B.MLA_ERR_ARG
 
 
+def no_gpu():
+    """Cases whose arguments pass validation carry fake pointers: run them
+    only where no GPU is visible, so the call stops at the device check and
+    never launches."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("valid arguments on fake pointers would launch on a GPU")
+
+
 def test_bf16_k_scale_is_ignored_not_rejected(split_plan):
     # a bf16 cache ignores k_scale (any value passes validation); without a
     # GPU the call then stops at the device check
+    no_gpu()
     rc = call_decode(split_plan, k_scale=0.0)
     assert rc in (B.MLA_ERR_CUDA, B.MLA_ERR_UNSUPPORTED, B.MLA_OK)
 
@@ -111,3 +121,43 @@ def test_segment_capacity_limit():
     with pytest.raises(B.MlaError) as ei:
         B.mla_decode_plan(np.full(5000, 10, dtype=np.int32), 64, 16, 1, num_sms=148)
     assert ei.value.code == B.MLA_ERR_ARG
+
+
+def call_bt_tokens(**over):
+    kw = dict(pool=FAKE, rows=10, cols=640, idx=FAKE, lens=FAKE, batch=3, page=64, bt=FAKE, mb=10)
+    kw.update(over)
+    return B.load().mla_block_table_from_tokens(kw["pool"], kw["rows"], kw["cols"], kw["idx"], kw["lens"],
+                                                kw["batch"], kw["page"], kw["bt"], kw["mb"], None)
+
+
+def call_bt_pages(**over):
+    kw = dict(pool=FAKE, rows=10, cols=10, idx=FAKE, batch=3, bt=FAKE, mb=10)
+    kw.update(over)
+    return B.load().mla_block_table_from_pages(kw["pool"], kw["rows"], kw["cols"], kw["idx"], kw["batch"],
+                                               kw["bt"], kw["mb"], None)
+
+
+@pytest.mark.parametrize("over", [
+    dict(page=16), dict(page=128), dict(lens=None), dict(lens=FAKE + 2), dict(pool=None), dict(idx=None),
+    dict(bt=None), dict(batch=0), dict(mb=0), dict(mb=B.MLA_BLOCK_TABLE_MAX_BLOCKS + 1), dict(rows=0),
+    dict(cols=0), dict(rows=1 << 40, cols=1 << 40), dict(bt=FAKE + 1),
+])
+def test_block_table_from_tokens_rejects(over):
+    assert call_bt_tokens(**over) == B.MLA_ERR_ARG
+    assert B.load().mla_decode_last_error_string()
+
+
+@pytest.mark.parametrize("over", [
+    dict(pool=None), dict(idx=None), dict(bt=None), dict(batch=-1), dict(mb=0), dict(rows=0), dict(cols=-5),
+    dict(idx=FAKE + 3),
+])
+def test_block_table_from_pages_rejects(over):
+    assert call_bt_pages(**over) == B.MLA_ERR_ARG
+
+
+def test_block_table_valid_args_reach_device_check():
+    # valid arguments pass validation; without a GPU the call then stops at
+    # the device check (never at a launch)
+    no_gpu()
+    assert call_bt_tokens() in (B.MLA_ERR_CUDA, B.MLA_ERR_UNSUPPORTED, B.MLA_OK)
+    assert call_bt_pages() in (B.MLA_ERR_CUDA, B.MLA_ERR_UNSUPPORTED, B.MLA_OK)
