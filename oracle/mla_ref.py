@@ -32,6 +32,12 @@ into (no blocking, no split-KV, no online softmax).  For request ``b`` with
 5. ``out = sum_j softmax(s)_j * row_j[:512]`` (``head_dim_v = kv_lora_rank``
    in ``flash_mla_with_kvcache``) and ``lse = ln sum_j exp(s_j)``.
 
+``mla_decode_ragged`` is the same decode with a different number of query
+tokens per request (packed by ``cu_seqlens_q``); token i of a request with
+q_b tokens sees ``L - q_b + 1 + i`` keys, the result of the pages' pad /
+uniform decode / unpad route (pinned against that route in
+tests/test_oracle_ragged.py).
+
 Readings taken where the pages are silent: lse uses the natural log and
 includes the scale; the FP8 value scale equals k_scale (the latent row is both
 key and value); the stored query stays bf16.
@@ -146,6 +152,50 @@ def mla_decode(
             v = max(n - q_len + 1 + i, 0)
             out[tok], lse[tok] = attend(
                 decode_bf16(q_nope_bits[tok]), decode_bf16(q_pe_bits[tok]), rows[:v], scale
+            )
+    return out, lse
+
+
+def mla_decode_ragged(
+    q_nope_bits: np.ndarray,
+    q_pe_bits: np.ndarray,
+    kv_bits: np.ndarray,
+    kv_dtype: str,
+    block_table: np.ndarray,
+    seq_lens: np.ndarray,
+    cu_seqlens_q: np.ndarray,
+    page_size: int,
+    scale: float,
+    k_scale: float = 1.0,
+):
+    """Reference decode with a different number of query tokens per request
+    (draft extend with a varying count of accepted drafts).
+
+    Query tokens of request b are rows ``cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1``
+    of ``q_*_bits [T,H,*]`` (sglang ``trtllm_mla_backend.py``,
+    ``init_forward_metadata``, draft-extend branch: ``cu_seqlens_q`` is the
+    zero-prefixed cumulative sum of ``extend_seq_lens``).  With ``q_b`` tokens
+    and ``L = seq_lens[b]`` cache tokens (its own new tokens included), token
+    i < q_b sees ``V = L - q_b + 1 + i`` keys: the pages pad every request's
+    queries to ``max_q`` rows, run the uniform decode with ``seq_lens_k = L -
+    q_b + max_q`` (same file, draft-extend branch and ``forward_extend``:
+    ``pad_draft_extend_query`` / ``unpad_draft_extend_output``), and keep
+    the first ``q_b`` rows, whose bottom-right causal rule gives that count.
+    Returns float64 (out [T,H,512], lse [T,H]); rows no request owns stay NaN.
+    """
+    t, h, _ = q_nope_bits.shape
+    out = np.full((t, h, KV_LORA_RANK), np.nan)
+    lse = np.full((t, h), np.nan)
+    dq = k_scale if kv_dtype == "e4m3" else 1.0
+    for b in range(len(seq_lens)):
+        n = int(seq_lens[b])
+        t0, t1 = int(cu_seqlens_q[b]), int(cu_seqlens_q[b + 1])
+        q_b = t1 - t0
+        rows = decode(gather_rows(kv_bits, block_table[b], n, page_size), kv_dtype) * dq
+        for i in range(q_b):
+            v = max(n - q_b + 1 + i, 0)
+            out[t0 + i], lse[t0 + i] = attend(
+                decode_bf16(q_nope_bits[t0 + i]), decode_bf16(q_pe_bits[t0 + i]), rows[:v], scale
             )
     return out, lse
 

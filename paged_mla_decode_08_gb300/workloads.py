@@ -68,6 +68,18 @@ CONFIGS = {
 }
 
 
+# Ragged query lengths: draft extend after speculative decoding, where each
+# request keeps a different number of accepted draft tokens (1..4 here, the
+# usual MTP draft width), 16 heads per GPU as in the q_len=4 verify case.
+RAGGED_CONFIGS = {
+    "draft_extend": dict(
+        batch=128, q_len_range=(1, 4), num_heads=16, page_size=64, kv_dtype="bf16",
+        seq_len_uniform=(2048, 8192), pool_pages=16384, k_scale=1.0,
+        desc="B=128, ragged q_len~U{1..4} causal (cu_seqlens_q), H=16, L~U[2048,8192], page 64",
+    ),
+}
+
+
 @dataclass
 class Workload:
     """One batch of decode inputs, as stored bit patterns on the host."""
@@ -86,10 +98,21 @@ class Workload:
     q_pe_bits: np.ndarray  # uint16 [T, H, 64] (bf16 bits)
     kv_bits: np.ndarray  # uint16 (bf16) or uint8 (e4m3) [P, page, 576]
     meta: dict = field(default_factory=dict)
+    # ragged query lengths (draft extend): tokens of request b are rows
+    # cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1; q_len is then their maximum
+    cu_seqlens_q: np.ndarray | None = None  # int32 [B + 1]
 
     @property
     def num_tokens(self) -> int:
+        if self.cu_seqlens_q is not None:
+            return int(self.cu_seqlens_q[-1])
         return self.batch * self.q_len
+
+    def q_lens(self) -> np.ndarray:
+        """Query tokens of each request."""
+        if self.cu_seqlens_q is not None:
+            return np.diff(self.cu_seqlens_q).astype(np.int32)
+        return np.full(self.batch, self.q_len, dtype=np.int32)
 
     @property
     def num_pages(self) -> int:
@@ -254,6 +277,37 @@ def make_workload(name: str, seed: int = 0, fill: str = "zero", **overrides) -> 
                           bt_pad_value=bt_pad_value, bt_extra_cols=bt_extra_cols)
 
 
+def make_ragged_workload(name: str = "draft_extend", seed: int = 0, q_lens=None, fill: str = "zero",
+                         **overrides) -> Workload:
+    """A workload whose requests carry different numbers of query tokens
+    (``q_lens``, drawn from the config's ``q_len_range`` when not given),
+    packed back to back; ``overrides`` replace config keys as in
+    ``make_workload``."""
+    cfg = dict(RAGGED_CONFIGS[name])
+    bt_pad_value = overrides.pop("bt_pad_value", -1)
+    bt_extra_cols = overrides.pop("bt_extra_cols", 0)
+    if "seq_lens" in overrides:
+        cfg.pop("seq_len_uniform", None)
+    cfg.update(overrides)
+    if "seq_lens" in cfg:
+        cfg["batch"] = len(cfg["seq_lens"])
+    b = cfg["batch"]
+    if q_lens is None:
+        lo, hi = cfg["q_len_range"]
+        q_lens = np.random.default_rng(seed + 7919).integers(lo, hi + 1, size=b)
+    q_lens = np.asarray(q_lens, dtype=np.int32)
+    assert q_lens.shape == (b,) and q_lens.min(initial=0) >= 0
+    cfg["q_len"] = max(int(q_lens.max(initial=1)), 1)
+    w = build_workload(name, cfg, seed=seed, fill=fill, bt_pad_value=bt_pad_value, bt_extra_cols=bt_extra_cols)
+    cu = np.zeros(b + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(q_lens)
+    t = int(cu[-1])
+    w.q_nope_bits = w.q_nope_bits[:t]
+    w.q_pe_bits = w.q_pe_bits[:t]
+    w.cu_seqlens_q = cu
+    return w
+
+
 def workload_stats(w: Workload) -> dict:
     """Algorithmic work of one decode step over ``w`` (per-unit figures:
     per visible KV token of a request, 576 stored elements are read once and
@@ -263,8 +317,9 @@ def workload_stats(w: Workload) -> dict:
     kv_tokens = int(lens.sum())
     # causal q_len>1: query i of a request sees L - q_len + 1 + i keys
     vis = 0
+    ql = w.q_lens().astype(np.int64)
     for i in range(w.q_len):
-        vis += int(np.maximum(lens - w.q_len + 1 + i, 0).sum())
+        vis += int(np.where(i < ql, np.maximum(lens - ql + 1 + i, 0), 0).sum())
     h = w.num_heads
     t = w.num_tokens
     kv_bytes = kv_tokens * KV_DIM * w.kv_elem_bytes
