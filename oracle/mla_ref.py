@@ -104,6 +104,14 @@ def gather_rows(kv_bits: np.ndarray, bt_row: np.ndarray, n: int, page_size: int)
     return kv_bits[pages, j % page_size]
 
 
+def request_rows(kv_bits: np.ndarray, kv_dtype: str, bt_row: np.ndarray, n: int, page_size: int,
+                 k_scale: float) -> np.ndarray:
+    """Dequantised float64 cache rows 0..n-1 of one request: an FP8 cache
+    scales by k_scale, a bf16 cache is taken as stored."""
+    dq = k_scale if kv_dtype == "e4m3" else 1.0
+    return decode(gather_rows(kv_bits, bt_row, n, page_size), kv_dtype) * dq
+
+
 def attend(qn: np.ndarray, qp: np.ndarray, rows: np.ndarray, scale: float):
     """Softmax attention of query heads ``qn [H,512]``, ``qp [H,64]`` over
     cache rows ``rows [V,576]`` (float64).  Returns (out [H,512], lse [H])."""
@@ -142,11 +150,10 @@ def mla_decode(
     t, h, _ = q_nope_bits.shape
     out = np.full((t, h, KV_LORA_RANK), np.nan)
     lse = np.full((t, h), np.nan)
-    dq = k_scale if kv_dtype == "e4m3" else 1.0
     reqs = range(len(seq_lens)) if requests is None else requests
     for b in reqs:
         n = int(seq_lens[b])
-        rows = decode(gather_rows(kv_bits, block_table[b], n, page_size), kv_dtype) * dq
+        rows = request_rows(kv_bits, kv_dtype, block_table[b], n, page_size, k_scale)
         for i in range(q_len):
             tok = b * q_len + i
             v = max(n - q_len + 1 + i, 0)
@@ -186,12 +193,11 @@ def mla_decode_ragged(
     t, h, _ = q_nope_bits.shape
     out = np.full((t, h, KV_LORA_RANK), np.nan)
     lse = np.full((t, h), np.nan)
-    dq = k_scale if kv_dtype == "e4m3" else 1.0
     for b in range(len(seq_lens)):
         n = int(seq_lens[b])
         t0, t1 = int(cu_seqlens_q[b]), int(cu_seqlens_q[b + 1])
         q_b = t1 - t0
-        rows = decode(gather_rows(kv_bits, block_table[b], n, page_size), kv_dtype) * dq
+        rows = request_rows(kv_bits, kv_dtype, block_table[b], n, page_size, k_scale)
         for i in range(q_b):
             v = max(n - q_b + 1 + i, 0)
             out[t0 + i], lse[t0 + i] = attend(
