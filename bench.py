@@ -303,6 +303,8 @@ def our_arm(args, w, rank, world):
     e2e = e2e_measure(db, w, dev, stream, max(3, min(K, 200)))
     # ---- the step before the decode: block-table construction, timed alone
     bt_rows = block_table_measure(w, dev, stream, flush, max(3, min(K, 200)))
+    # ---- ragged query counts (draft extend), the same decode kernels
+    ragged = ragged_measure(dev, stream, flush, max(3, min(K, 200)), peaks)
 
     if rank != 0:
         return
@@ -345,6 +347,7 @@ def our_arm(args, w, rank, world):
         "t_roof_us": {"hbm": t_hbm * 1e6, "tensor": t_tc * 1e6},
         "wall_s_timed_loop": wall,
         "block_table_build": bt_rows,
+        "ragged_decode": ragged,
         "segments": int(len(db.plan.segments())), "partial_slots": db.plan.num_partial_slots,
         "kernel_source_sha": kernel_source_hash(),
     }
@@ -393,6 +396,32 @@ def block_table_measure(w, dev, stream, flush, K):
     got = bt.cpu().numpy()
     res["last_table_matches_workload"] = bool(np.array_equal(got, want))
     return res
+
+
+def ragged_measure(dev, stream, flush, K, peaks):
+    """The draft-extend workload (per-request query counts 1..4 packed by
+    cu_seqlens_q), one mla_decode_ragged call per step between events after
+    an L2 flush; roofline against the same HBM peak as the main line."""
+    import torch
+    from paged_mla_decode_08_gb300 import runner as R
+    w = W.make_ragged_workload("draft_extend", seed=0)
+    st = W.workload_stats(w)
+    db = R.upload(w, device=dev)
+    for _ in range(3):
+        R.decode(db, stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        R.decode(db, stream)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    s_avg = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    gbs = st["alg_bytes"] / s_avg / 1e9
+    return {"workload": workload_desc(w)["workload"], "us": s_avg * 1e6, "tokens_per_s": st["tokens"] / s_avg,
+            "query_tokens": st["tokens"], "alg_bytes": st["alg_bytes"], "achieved_gbs": gbs,
+            "hbm_frac": gbs / float(peaks["hbm_gbs"]), "launches_per_step": 1 + (db.plan.num_partial_slots > 0),
+            "note": "decode step incl. combine; L2 flushed between steps"}
 
 
 def e2e_measure(db, w, dev, stream, K):

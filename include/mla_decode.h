@@ -158,6 +158,46 @@ int mla_decode_combine(const mla_plan* plan, void* out, float* lse, void* worksp
                        size_t workspace_bytes, void* stream);
 
 /*
+ * Ragged query counts: a batch whose requests carry different numbers of
+ * query tokens, packed back to back -- the draft-extend step after
+ * speculative decoding, where each request keeps a different number of
+ * accepted draft tokens (sglang trtllm_mla_backend.py, init_forward_metadata,
+ * draft-extend branch: cu_seqlens_q = [0, cumsum(extend_seq_lens)]).
+ *
+ * Token i < q_b of request b (query row cu_seqlens_q[b] + i) sees
+ *   V = L - q_b + 1 + i keys,  L = seq_lens[b],  q_b = cu_seqlens_q[b+1] - cu_seqlens_q[b],
+ * the same bottom-right causal rule as mla_decode per request: exactly what
+ * the pages obtain by padding every request's queries to the longest,
+ * decoding with seq_lens_k = L - q_b + max_q and dropping the padding rows
+ * (forward_extend, pad_draft_extend_query / unpad_draft_extend_output),
+ * without the padding.
+ *
+ * mla_decode_plan_ragged: as mla_decode_plan with q_len = max(q_lens_host)
+ * (at least 1; num_heads * that <= 128).  q_lens_host: host int32 [batch],
+ * >= 0 (0 = a request with no query token); only read during the call.  The
+ * device counts given to mla_decode_ragged may differ as long as none
+ * exceeds that maximum.
+ *
+ * mla_decode_ragged: as mla_decode, except
+ *   q_nope, q_pe, out, lse  hold num_tokens rows, 1 <= num_tokens <=
+ *                 batch * max(q_lens); rows no request owns are not written.
+ *   cu_seqlens_q  device int32 [batch + 1], nondecreasing, cu_seqlens_q[0] >= 0,
+ *                 cu_seqlens_q[batch] <= num_tokens, each count <= the
+ *                 planned maximum.  A request whose entry breaks this gets no
+ *                 query row (nothing is read or written for it) and the error
+ *                 word of mla_decode_device_error reads 0x501.
+ * Errors: those of mla_decode; MLA_ERR_ARG also for a NULL cu_seqlens_q.
+ * (mla_decode_main / mla_decode_combine are the uniform path only.)
+ */
+int mla_decode_plan_ragged(const int32_t* seq_lens_host, const int32_t* q_lens_host, int batch, int page_size,
+                           int num_heads, int num_sms, mla_plan** plan_out, size_t* workspace_bytes_out);
+int mla_decode_ragged(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_tokens, int num_heads,
+                      const void* kv_pages, int kv_dtype, int64_t num_pages, int page_size,
+                      const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                      const int32_t* cu_seqlens_q, float scale, float k_scale, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mla_decode_noalloc -- the decode for callers that cannot allocate device
  * memory.  (No counterpart on the serving pages: their backends always own a
  * workspace buffer; this entry point is this library's own addition.)

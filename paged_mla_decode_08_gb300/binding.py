@@ -37,6 +37,9 @@ SIGNATURES = {
     "mla_decode_main": (_c_int, _DECODE_ARGS),
     "mla_decode_combine": (_c_int, [_vp, _vp, _vp, _vp, _c_size, _vp]),
     "mla_decode_noalloc": (_c_int, _DECODE_ARGS[:16] + [_vp]),
+    "mla_decode_plan_ragged": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_vp),
+                                        ctypes.POINTER(_c_size)]),
+    "mla_decode_ragged": (_c_int, _DECODE_ARGS[:12] + [_vp] + _DECODE_ARGS[12:]),
     "mla_block_table_from_tokens": (_c_int, [_vp, ctypes.c_int64, ctypes.c_int64, _vp, _vp, _c_int, _c_int,
                                              _vp, _c_int, _vp]),
     "mla_block_table_from_pages": (_c_int, [_vp, ctypes.c_int64, ctypes.c_int64, _vp, _c_int, _vp, _c_int,
@@ -145,6 +148,20 @@ def mla_decode_plan(seq_lens_host, page_size: int, num_heads: int, q_len: int = 
     return Plan(handle.value, ws.value, int(lens.shape[0]), page_size, num_heads, q_len)
 
 
+def mla_decode_plan_ragged(seq_lens_host, q_lens_host, page_size: int, num_heads: int, num_sms: int = 0) -> Plan:
+    """Plan a batch whose requests carry ``q_lens_host[b]`` query tokens each."""
+    lib = load()
+    lens = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+    qls = np.ascontiguousarray(np.asarray(q_lens_host, dtype=np.int32))
+    if qls.shape != lens.shape:
+        raise MlaError(MLA_ERR_ARG, "q_lens and seq_lens differ in length")
+    handle = _vp()
+    ws = _c_size()
+    _check(lib.mla_decode_plan_ragged(lens.ctypes.data_as(_i32p), qls.ctypes.data_as(_i32p), int(lens.shape[0]),
+                                      page_size, num_heads, num_sms, ctypes.byref(handle), ctypes.byref(ws)))
+    return Plan(handle.value, ws.value, int(lens.shape[0]), page_size, num_heads, max(int(qls.max(initial=1)), 1))
+
+
 def _decode_args(plan, q_nope, q_pe, kv_pages, kv_dtype, block_table, seq_lens, scale, k_scale,
                  out, lse, workspace, workspace_bytes, stream):
     num_pages = kv_pages.shape[0]
@@ -162,6 +179,15 @@ def mla_decode(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_table, s
     """Decode into ``out`` / ``lse`` (torch CUDA tensors) on ``stream``."""
     _check(load().mla_decode(*_decode_args(plan, q_nope, q_pe, kv_pages, kv_dtype, block_table, seq_lens,
                                            scale, k_scale, out, lse, workspace, workspace_bytes, stream)))
+
+
+def mla_decode_ragged(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_table, seq_lens, cu_seqlens_q,
+                      scale: float, k_scale: float, out, lse, workspace=None, workspace_bytes=None, stream=None):
+    """Decode a ragged batch (query rows of request b: cu_seqlens_q[b] ..
+    cu_seqlens_q[b+1]-1) into ``out`` / ``lse``."""
+    args = _decode_args(plan, q_nope, q_pe, kv_pages, kv_dtype, block_table, seq_lens, scale, k_scale, out, lse,
+                        workspace, workspace_bytes, stream)
+    _check(load().mla_decode_ragged(*args[:12], _ptr(cu_seqlens_q), *args[12:]))
 
 
 def mla_decode_main(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_table, seq_lens, scale: float,

@@ -2,6 +2,7 @@
 // Every argument error is caught here, on the host, before any launch.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstdio>
@@ -74,18 +75,23 @@ struct Prepared {
   mla::DecodeArgs args;
 };
 
+// cu_seqlens_q: NULL for a uniform batch (num_tokens = batch * q_len), else
+// the ragged query offsets (1 <= num_tokens <= batch * planned maximum).
 int prepare(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_tokens, int num_heads,
             const void* kv_pages, int kv_dtype, int64_t num_pages, int page_size,
-            const int32_t* block_table, int bt_stride, const int32_t* seq_lens, float scale,
-            float k_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+            const int32_t* block_table, int bt_stride, const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+            float scale, float k_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
             Prepared* pr) {
   if (!plan) return fail(MLA_ERR_ARG, "plan is NULL");
   if (!q_nope || !q_pe || !kv_pages || !block_table || !seq_lens || !out || !lse)
     return fail(MLA_ERR_ARG, "a required device pointer is NULL");
-  if (num_tokens != plan->batch * plan->q_len || num_heads != plan->num_heads ||
-      page_size != plan->page_size)
+  const bool tokens_ok = cu_seqlens_q ? (num_tokens >= 1 && num_tokens <= plan->batch * plan->q_len)
+                                      : num_tokens == plan->batch * plan->q_len;
+  if (!tokens_ok || num_heads != plan->num_heads || page_size != plan->page_size)
     return fail(MLA_ERR_PLAN_MISMATCH,
                 "num_tokens / num_heads / page_size differ from the plan (re-plan for this batch)");
+  if (cu_seqlens_q && !aligned(cu_seqlens_q, 4)) return fail(MLA_ERR_ARG, "cu_seqlens_q must be 4-byte aligned");
+  if ((int64_t)num_tokens * num_heads > INT32_MAX) return fail(MLA_ERR_ARG, "num_tokens * num_heads must be < 2^31");
   if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_E4M3) return fail(MLA_ERR_ARG, "kv_dtype must be MLA_KV_BF16 or MLA_KV_E4M3");
   if (num_pages <= 0) return fail(MLA_ERR_ARG, "num_pages must be > 0");
   if (num_pages * (int64_t)page_size > INT32_MAX) return fail(MLA_ERR_ARG, "num_pages * page_size must be < 2^31");
@@ -113,6 +119,8 @@ int prepare(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_
   a.batch = plan->batch; a.q_len = plan->q_len; a.num_heads = plan->num_heads; a.rows = plan->rows;
   a.score_scale_log2 = (float)((double)scale * (double)kf * 1.4426950408889634);
   a.out_scale = kf;
+  a.cu_q = cu_seqlens_q;
+  a.num_tokens = num_tokens;
   return MLA_OK;
 }
 
@@ -171,7 +179,8 @@ int mla_decode_main(const mla_plan* plan, const void* q_nope, const void* q_pe, 
                     void* stream) {
   Prepared pr;
   int rc = prepare(plan, q_nope, q_pe, num_tokens, num_heads, kv_pages, kv_dtype, num_pages, page_size,
-                   block_table, bt_stride, seq_lens, scale, k_scale, out, lse, workspace, workspace_bytes, &pr);
+                   block_table, bt_stride, seq_lens, nullptr, scale, k_scale, out, lse, workspace, workspace_bytes,
+                   &pr);
   if (rc != MLA_OK) return rc;
   rc = check_device(nullptr);
   if (rc != MLA_OK) return rc;
@@ -206,7 +215,46 @@ int mla_decode(const mla_plan* plan, const void* q_nope, const void* q_pe, int n
                void* workspace, size_t workspace_bytes, void* stream) {
   Prepared pr;
   int rc = prepare(plan, q_nope, q_pe, num_tokens, num_heads, kv_pages, kv_dtype, num_pages, page_size,
-                   block_table, bt_stride, seq_lens, scale, k_scale, out, lse, workspace, workspace_bytes, &pr);
+                   block_table, bt_stride, seq_lens, nullptr, scale, k_scale, out, lse, workspace, workspace_bytes,
+                   &pr);
+  if (rc != MLA_OK) return rc;
+  rc = check_device(nullptr);
+  if (rc != MLA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = launch_main(plan, pr, s);
+  if (rc != MLA_OK) return rc;
+  rc = launch_combine(plan, pr, s);
+  return rc == MLA_OK ? ok() : rc;
+}
+
+int mla_decode_plan_ragged(const int32_t* seq_lens_host, const int32_t* q_lens_host, int batch, int page_size,
+                           int num_heads, int num_sms, mla_plan** plan_out, size_t* workspace_bytes_out) {
+  if (!plan_out) return fail(MLA_ERR_ARG, "plan_out is NULL");
+  *plan_out = nullptr;
+  if (!q_lens_host) return fail(MLA_ERR_ARG, "q_lens_host is NULL");
+  if (batch < 1) return fail(MLA_ERR_ARG, "batch must be >= 1");
+  int q_max = 1;
+  for (int b = 0; b < batch; ++b) {
+    if (q_lens_host[b] < 0) return fail(MLA_ERR_ARG, "q_lens must be >= 0");
+    q_max = std::max(q_max, (int)q_lens_host[b]);
+  }
+  int rc = mla_decode_plan(seq_lens_host, batch, page_size, num_heads, q_max, num_sms, plan_out,
+                           workspace_bytes_out);
+  if (rc != MLA_OK) return rc;
+  (*plan_out)->ragged = true;
+  return ok();
+}
+
+int mla_decode_ragged(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_tokens, int num_heads,
+                      const void* kv_pages, int kv_dtype, int64_t num_pages, int page_size,
+                      const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                      const int32_t* cu_seqlens_q, float scale, float k_scale, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!cu_seqlens_q) return fail(MLA_ERR_ARG, "cu_seqlens_q is NULL");
+  Prepared pr;
+  int rc = prepare(plan, q_nope, q_pe, num_tokens, num_heads, kv_pages, kv_dtype, num_pages, page_size,
+                   block_table, bt_stride, seq_lens, cu_seqlens_q, scale, k_scale, out, lse, workspace,
+                   workspace_bytes, &pr);
   if (rc != MLA_OK) return rc;
   rc = check_device(nullptr);
   if (rc != MLA_OK) return rc;

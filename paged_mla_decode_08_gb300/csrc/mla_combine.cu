@@ -46,10 +46,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
   // visible; without the launch attribute it returns at once).
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const CombineJob job = jobs.job[blockIdx.x];
-  const int M = a.rows;
+  const int M = a.rows;  // partial-row stride: the planned rows per request
   const int r0 = blockIdx.y * kCombRows;
   const int c0 = blockIdx.z * kCombChunks;
-  const int nrows = min(kCombRows, M - r0);
+  // this request's query rows (fewer than M in a ragged batch) and where
+  // they go in out / lse
+  const int2 q = request_q(a, job.req);
+  const int nrows = min(kCombRows, q.y * a.num_heads - r0);
+  if (nrows <= 0) return;  // whole CTA: no row of this block belongs to the request
+  const size_t orow0 = (size_t)q.x * a.num_heads + r0;
   __shared__ uint4 s_out[kCombRows][kCombChunks + 1];
 
   const int r = threadIdx.x & 31;  // row within the block
@@ -74,7 +79,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
       for (int s = 0; s < job.nsplit; ++s) mx = fmaxf(mx, __ldg(pl + (size_t)s * M));
       if (mx != -CUDART_INF_F)
         for (int s = 0; s < job.nsplit; ++s) tot += __expf(__ldg(pl + (size_t)s * M) - mx);
-      if (blockIdx.z == 0) a.lse[(size_t)job.req * M + r0 + r] = tot > 0.f ? mx + __logf(tot) : -CUDART_INF_F;
+      if (blockIdx.z == 0) a.lse[orow0 + r] = tot > 0.f ? mx + __logf(tot) : -CUDART_INF_F;
     }
     const float inv = tot > 0.f ? 1.f / tot : 0.f;
     for (int s = 0; s < job.nsplit; ++s) {
@@ -131,7 +136,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
   // 32 rows x 256 bytes: a half-warp writes one row segment (16 lanes x 16 B)
   const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
   for (int rr = hw; rr < nrows; rr += 16) {
-    const size_t row = (size_t)job.req * M + r0 + rr;
+    const size_t row = orow0 + rr;
     uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * kLatent + kChunkCols * c0) + l16;
     *dst = s_out[rr][l16];
   }

@@ -78,13 +78,34 @@ struct DecodeArgs {
   int32_t rows;        // M = num_heads * q_len
   float score_scale_log2;  // scale * kf * log2(e): logits in base-2 units
   float out_scale;         // kf (value dequantisation)
+  const int32_t* cu_q;     // ragged batches: int32 [batch + 1] first query token of each
+                           // request (q_len is then the planned maximum); nullptr: uniform
+  int32_t num_tokens;      // rows of q_nope / q_pe / out / lse
 };
+
+#ifdef __CUDACC__
+// First query token and query-token count of request b: (b * q_len, q_len)
+// for a uniform batch; (cu_q[b], cu_q[b+1] - cu_q[b]) for a ragged one.  A
+// ragged entry outside 0 <= cu_q[b] <= cu_q[b+1] <= num_tokens, or with more
+// tokens than the planned maximum, counts as no query token (*bad is set),
+// so no access leaves the query and output arrays.
+__device__ __forceinline__ int2 request_q(const DecodeArgs& a, int b, bool* bad = nullptr) {
+  if (a.cu_q == nullptr) return make_int2(b * a.q_len, a.q_len);
+  const int t0 = __ldg(a.cu_q + b), t1 = __ldg(a.cu_q + b + 1);
+  if (t0 < 0 || t1 < t0 || t1 > a.num_tokens || t1 - t0 > a.q_len) {
+    if (bad) *bad = true;
+    return make_int2(0, 0);
+  }
+  return make_int2(t0, t1 - t0);
+}
+#endif
 
 }  // namespace mla
 
 // The plan object behind the opaque C handle.
 struct mla_plan {
   int batch = 0, page_size = 0, num_heads = 0, q_len = 0, rows = 0;
+  bool ragged = false;  // planned from per-request query counts (q_len = their maximum)
   int num_sms = 0, num_workers = 0;
   int max_pages = 0;  // ceil(max seq_len / page_size)
   int num_slots = 0;

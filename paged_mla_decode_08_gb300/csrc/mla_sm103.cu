@@ -88,7 +88,8 @@ constexpr int OFF_SINK = OFF_RED + 4 * 2 * 128 * 4;      // per slot 128 words: 
 constexpr int kNoteBytes = 128 * 4;
 constexpr int OFF_SEGLEN = OFF_SINK + kSlots * kNoteBytes;  // key counts of the worker's first segments
 constexpr int kSegLenCache = 64;
-constexpr int OFF_BAR = OFF_SEGLEN + kSegLenCache * 4;
+constexpr int OFF_SEGQ = OFF_SEGLEN + kSegLenCache * 4;     // ... and their (first token, query count)
+constexpr int OFF_BAR = OFF_SEGQ + kSegLenCache * 8;
 enum Bar : int {
   B_KV_FULL = 0, B_KV_EMPTY = B_KV_FULL + kStages, B_S_FULL = B_KV_EMPTY + kStages, B_P_FULL = B_S_FULL + 2,
   B_PV_DONE, B_Q_READY, B_X_FULL, B_X_EMPTY = B_X_FULL + kSlots, B_TAIL = B_X_EMPTY + kSlots, B_FINAL,
@@ -123,6 +124,7 @@ struct Ctx {
   uint32_t sbase;    // its shared-window address
   volatile int* abort_flag;
   const int* seg_len;  // request_len() of segments seg0 .. seg0 + kSegLenCache - 1
+  const int2* seg_q;   // request_q() of the same segments
   int seg0;
   __device__ uint32_t bar(int i) const { return sbase + OFF_BAR + 8 * i; }
 };
@@ -169,6 +171,27 @@ __device__ __forceinline__ int seg_len(const Ctx& c, const Schedule<CAP>& sched,
   return k < kSegLenCache ? c.seg_len[k] : request_len(a, sched.seg[s].req);
 }
 
+// request_q() with a malformed ragged entry recorded in the error word
+__device__ __forceinline__ int2 request_q_checked(const DecodeArgs& a, int b) {
+  bool bad = false;
+  const int2 q = request_q(a, b, &bad);
+  if (bad) atomicCAS(&g_kernel_error, 0, 0x501);
+  return q;
+}
+
+// (first query token, query count) of schedule segment s, cached like seg_len
+template <int CAP>
+__device__ __forceinline__ int2 seg_q(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, int s) {
+  const int k = s - c.seg0;
+  return k < kSegLenCache ? c.seg_q[k] : request_q_checked(a, sched.seg[s].req);
+}
+
+// Row of out / lse that query row `row` of a request with (first token,
+// query count) q writes, or -1 when the request has fewer rows.
+__device__ __forceinline__ int out_row(int2 q, int num_heads, int row) {
+  return row < q.y * num_heads ? q.x * num_heads + row : -1;
+}
+
 __device__ __forceinline__ int segment_tiles(const Segment& sg, int L) {
   const int last = (L + kTileTokens - 1) / kTileTokens;
   const int e = sg.tile_end < last ? sg.tile_end : last;
@@ -211,12 +234,15 @@ __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeA
     };
     if (nt > 0 && lane == 0) {
       // the exchange warps load this request's query when the segment
-      // starts: pull it into L2 now, a few tiles ahead (the M rows are
+      // starts: pull it into L2 now, a few tiles ahead (its rows are
       // contiguous; 16-byte multiples)
-      prefetch_l2_bulk(reinterpret_cast<const __nv_bfloat16*>(a.q_nope) + (size_t)sg.req * a.rows * kLatent,
-                       (uint32_t)a.rows * kLatent * 2);
-      prefetch_l2_bulk(reinterpret_cast<const __nv_bfloat16*>(a.q_pe) + (size_t)sg.req * a.rows * kRope,
-                       (uint32_t)a.rows * kRope * 2);
+      const int2 q = seg_q(c, sched, a, s);
+      const size_t r0 = (size_t)q.x * a.num_heads;
+      const uint32_t nr = (uint32_t)(q.y * a.num_heads);
+      if (nr > 0) {
+        prefetch_l2_bulk(reinterpret_cast<const __nv_bfloat16*>(a.q_nope) + r0 * kLatent, nr * kLatent * 2);
+        prefetch_l2_bulk(reinterpret_cast<const __nv_bfloat16*>(a.q_pe) + r0 * kRope, nr * kRope * 2);
+      }
     }
     for (int jj = 0; jj < nt; ++jj, ++j) {
       const int stage = j % (F8 ? kF8Stages : kStages);
@@ -530,11 +556,13 @@ __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const Decode
     // piece into TMEM; the rope rows go straight to their final layout.
     {
       const int ql = lane >> 2, qc = lane & 3;  // load mapping: row 8k + ql, 16-byte chunk qc
-      const size_t row0 = (size_t)sg.req * M + 32 * quad;
+      const int2 q = seg_q(c, sched, a, s);
+      const int rows_b = q.y * a.num_heads;     // this request's query rows (<= M; the rest stay 0)
+      const size_t row0 = (size_t)q.x * a.num_heads + 32 * quad;
       const uint4* qn = reinterpret_cast<const uint4*>(a.q_nope) + row0 * (kLatent / 8) + 32 * rank + qc;
       const uint4* qp = reinterpret_cast<const uint4*>(a.q_pe) + row0 * (kRope / 8) + 4 * rank + qc;
       const uint32_t stage = c.sbase + OFF_QROPE + quad * 2048;  // this warp's rows of the rope area
-      auto lrow_ok = [&](int rl) { return 32 * quad + rl < M; };
+      auto lrow_ok = [&](int rl) { return 32 * quad + rl < rows_b; };
       auto cvt4 = [&](uint4 v) {
         return F8 ? make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w))
                   : v;
@@ -655,10 +683,16 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
 
   for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
     const Segment sg = sched.seg[s];
-    const int b = sg.req;
     const int L = seg_len(c, sched, a, s);
     const int nt = segment_tiles(sg, L);
-    const int vis = valid_row ? L - a.q_len + 1 + qi : 0;  // visible keys of this row
+    // visible keys of this row; rows past the request's query rows (ragged
+    // batches) still take part in the exchange with the peer but see no key
+    // and write nothing
+    int vis;
+    {
+      const int2 q = seg_q(c, sched, a, s);
+      vis = row < q.y * a.num_heads ? L - q.y + 1 + qi : 0;
+    }
     float m_ref = -CUDART_INF_F, l = 0.f;
 
     if (nt > 0) {
@@ -788,7 +822,10 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
       ++nseg;
     }
     {
-      const size_t orow = (size_t)b * M + row;
+      // output row of this thread's query row, -1 past the request's rows
+      // (re-read from the cache: nothing is held across the tile loop)
+      const int orow = out_row(seg_q(c, sched, a, s), a.num_heads, row);
+      const bool live_row = orow >= 0;
       const bool live = l > 0.f;
       const float inv = live ? a.out_scale / l : 0.f;
 #pragma unroll 1
@@ -802,9 +839,9 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
           for (int v = 0; v < 32; ++v) o[v] = 0u;
         }
         const int col = 256 * rank + 128 * half + 32 * ck;
-        if (!valid_row) continue;
+        if (sg.slot < 0 ? !live_row : !valid_row) continue;
         if (sg.slot < 0) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * kLatent + col);
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + (size_t)orow * kLatent + col);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             float d0, d1;
@@ -833,8 +870,11 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
       }
       if (rank == 0 && half == 0 && valid_row) {
         const float lse = live ? (m_ref + __log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
-        if (sg.slot < 0) a.lse[orow] = lse;
-        else a.part_lse[(size_t)sg.slot * M + row] = lse;
+        if (sg.slot < 0) {
+          if (live_row) a.lse[orow] = lse;
+        } else {
+          a.part_lse[(size_t)sg.slot * M + row] = lse;
+        }
       }
     }
     tc_fence_before();
@@ -858,12 +898,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int rank = (int)cluster_ctarank();
   const int worker = blockIdx.x >> 1;
   c.seg_len = reinterpret_cast<const int*>(c.smem + OFF_SEGLEN);
+  c.seg_q = reinterpret_cast<const int2*>(c.smem + OFF_SEGQ);
   c.seg0 = worker < sched.num_workers ? sched.worker_seg[worker] : 0;
   if (warp == 2 && worker < sched.num_workers) {
-    // key counts of this worker's segments, read once for every role
+    // key counts and query rows of this worker's segments, read once for
+    // every role
     const int n = min(sched.worker_seg[worker + 1] - c.seg0, kSegLenCache);
-    for (int i = threadIdx.x & 31; i < n; i += 32)
-      reinterpret_cast<int*>(c.smem + OFF_SEGLEN)[i] = request_len(a, sched.seg[c.seg0 + i].req);
+    for (int i = threadIdx.x & 31; i < n; i += 32) {
+      const int req = sched.seg[c.seg0 + i].req;
+      reinterpret_cast<int*>(c.smem + OFF_SEGLEN)[i] = request_len(a, req);
+      reinterpret_cast<int2*>(c.smem + OFF_SEGQ)[i] = request_q_checked(a, req);
+    }
   }
 
   if (threadIdx.x == 0) {

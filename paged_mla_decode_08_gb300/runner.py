@@ -27,6 +27,7 @@ class DeviceBatch:
     out: torch.Tensor  # bf16 [T,H,512]
     lse: torch.Tensor  # fp32 [T,H]
     workspace: Optional[torch.Tensor]
+    cu_seqlens_q: Optional[torch.Tensor] = None  # int32 [B+1] for a ragged batch
 
 
 def _bits_to_bf16(a: np.ndarray, device) -> torch.Tensor:
@@ -37,7 +38,10 @@ def upload(w: Workload, device="cuda", num_sms: int = 0, plan_seq_lens=None) -> 
     """Copy ``w`` to ``device`` and plan it (``plan_seq_lens`` overrides the
     host lengths the plan is made from, e.g. upper bounds)."""
     lens = w.seq_lens if plan_seq_lens is None else np.asarray(plan_seq_lens, dtype=np.int32)
-    plan = B.mla_decode_plan(lens, w.page_size, w.num_heads, w.q_len, num_sms)
+    if w.cu_seqlens_q is not None:
+        plan = B.mla_decode_plan_ragged(lens, w.q_lens(), w.page_size, w.num_heads, num_sms)
+    else:
+        plan = B.mla_decode_plan(lens, w.page_size, w.num_heads, w.q_len, num_sms)
     if w.kv_dtype == "bf16":
         kv = _bits_to_bf16(w.kv_bits, device)
         kv_dtype = B.MLA_KV_BF16
@@ -57,12 +61,17 @@ def upload(w: Workload, device="cuda", num_sms: int = 0, plan_seq_lens=None) -> 
         out=torch.empty((t, h, KV_LORA_RANK), dtype=torch.bfloat16, device=device),
         lse=torch.empty((t, h), dtype=torch.float32, device=device),
         workspace=ws,
+        cu_seqlens_q=None if w.cu_seqlens_q is None else torch.from_numpy(w.cu_seqlens_q).to(device),
     )
 
 
 def decode(db: DeviceBatch, stream=None):
-    B.mla_decode(db.plan, db.q_nope, db.q_pe, db.kv, db.kv_dtype, db.block_table, db.seq_lens,
-                 db.w.scale, db.w.k_scale, db.out, db.lse, db.workspace, None, stream)
+    if db.cu_seqlens_q is not None:
+        B.mla_decode_ragged(db.plan, db.q_nope, db.q_pe, db.kv, db.kv_dtype, db.block_table, db.seq_lens,
+                            db.cu_seqlens_q, db.w.scale, db.w.k_scale, db.out, db.lse, db.workspace, None, stream)
+    else:
+        B.mla_decode(db.plan, db.q_nope, db.q_pe, db.kv, db.kv_dtype, db.block_table, db.seq_lens,
+                     db.w.scale, db.w.k_scale, db.out, db.lse, db.workspace, None, stream)
     return db.out, db.lse
 
 

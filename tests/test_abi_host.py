@@ -161,3 +161,55 @@ def test_block_table_valid_args_reach_device_check():
     no_gpu()
     assert call_bt_tokens() in (B.MLA_ERR_CUDA, B.MLA_ERR_UNSUPPORTED, B.MLA_OK)
     assert call_bt_pages() in (B.MLA_ERR_CUDA, B.MLA_ERR_UNSUPPORTED, B.MLA_OK)
+
+
+def call_ragged(plan, **over):
+    kw = dict(q_nope=FAKE, q_pe=FAKE, num_tokens=5, num_heads=plan.num_heads, kv=FAKE, kv_dtype=B.MLA_KV_BF16,
+              num_pages=100, page_size=plan.page_size, bt=FAKE, bt_stride=64, seq_lens=FAKE, cu=FAKE,
+              scale=0.07, k_scale=1.0, out=FAKE, lse=FAKE, ws=FAKE, ws_bytes=plan.workspace_bytes, stream=None)
+    kw.update(over)
+    return B.load().mla_decode_ragged(plan.handle, kw["q_nope"], kw["q_pe"], kw["num_tokens"], kw["num_heads"],
+                                      kw["kv"], kw["kv_dtype"], kw["num_pages"], kw["page_size"], kw["bt"],
+                                      kw["bt_stride"], kw["seq_lens"], kw["cu"], kw["scale"], kw["k_scale"],
+                                      kw["out"], kw["lse"], kw["ws"], kw["ws_bytes"], kw["stream"])
+
+
+@pytest.fixture
+def ragged_plan():
+    p = B.mla_decode_plan_ragged([4000, 3000, 100], [1, 4, 2], 64, 16, num_sms=148)
+    assert p.q_len == 4 and p.workspace_bytes > 0
+    return p
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(cu=None), B.MLA_ERR_ARG),
+    (dict(cu=FAKE + 2), B.MLA_ERR_ARG),
+    (dict(num_tokens=0), B.MLA_ERR_PLAN_MISMATCH),
+    (dict(num_tokens=13), B.MLA_ERR_PLAN_MISMATCH),   # > batch * max q_len = 12
+    (dict(num_heads=8), B.MLA_ERR_PLAN_MISMATCH),
+    (dict(ws_bytes=10), B.MLA_ERR_WORKSPACE),
+    (dict(q_pe=None), B.MLA_ERR_ARG),
+])
+def test_ragged_decode_rejects(ragged_plan, over, code):
+    assert call_ragged(ragged_plan, **over) == code
+
+
+def test_ragged_plan_rules():
+    # planned rows follow the largest query count; zero counts are allowed
+    p = B.mla_decode_plan_ragged([10, 20, 30], [0, 8, 3], 64, 16, num_sms=148)
+    assert p.q_len == 8
+    with pytest.raises(B.MlaError) as ei:
+        B.mla_decode_plan_ragged([10, 20], [1, 9], 64, 16, num_sms=148)   # 16 * 9 > 128 rows
+    assert ei.value.code == B.MLA_ERR_ARG
+    with pytest.raises(B.MlaError) as ei:
+        B.mla_decode_plan_ragged([10, 20], [1, -1], 64, 16, num_sms=148)
+    assert ei.value.code == B.MLA_ERR_ARG
+    # the schedule ignores query counts: same segments as the uniform plan
+    u = B.mla_decode_plan([4000, 3000, 100], 64, 16, 4, num_sms=148)
+    r = B.mla_decode_plan_ragged([4000, 3000, 100], [1, 4, 2], 64, 16, num_sms=148)
+    assert np.array_equal(u.segments(), r.segments()) and u.workspace_bytes == r.workspace_bytes
+
+
+def test_ragged_valid_args_reach_device_check(ragged_plan):
+    no_gpu()
+    assert call_ragged(ragged_plan) in (B.MLA_ERR_CUDA, B.MLA_ERR_UNSUPPORTED, B.MLA_OK)
