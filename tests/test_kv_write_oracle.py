@@ -1,0 +1,215 @@
+"""Pins of the RoPE + FP8 quantisation + cache-write oracle
+(oracle/kv_write_ref.py), CPU only.
+
+The pages show only the calls, so the pins are what the mathematics and the
+formats fix: rotations worked by hand for both pairings, the rotation's norm
+and relative-position properties on a RoFormer frequency table, e4m3
+rounding against the format's value table, its ties and saturation, and
+against torch's float8 conversion; the cache write round-trips through the
+decode oracle's gather.  ``test_planted_mistake_is_caught`` plants plausible
+mistakes (swapped sin sign, pairing swapped, truncation, ties away from zero,
+slot split by the wrong page size) and checks that a pin rejects each.
+"""
+
+import inspect
+import math
+import types
+
+import numpy as np
+import pytest
+
+from oracle import kv_write_ref as K
+from oracle import mla_ref as O
+
+
+def roformer_cache(max_pos, base=10000.0, dim=64):
+    """cos/sin table of RoFormer: theta_i = base^(-2i/dim), angle = p * theta_i."""
+    inv = base ** (-np.arange(0, dim, 2, dtype=np.float64) / dim)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1)
+
+
+def pin_hand_rotation(mod):
+    """Pair 0 rotated by 90 degrees, pair 1 by 180, the rest untouched
+    (cos 1, sin 0), for both pairings."""
+    cos = np.ones(32)
+    sin = np.zeros(32)
+    cos[0], sin[0] = 0.0, 1.0
+    cos[1], sin[1] = -1.0, 0.0
+    x = np.arange(1, 65, dtype=np.float64)
+    neox = mod.rotate(x, cos, sin, True)
+    want_neox = x.copy()
+    want_neox[0], want_neox[32] = -x[32], x[0]      # (a, b) -> (-b, a)
+    want_neox[1], want_neox[33] = -x[1], -x[33]     # (a, b) -> (-a, -b)
+    inter = mod.rotate(x, cos, sin, False)
+    want_inter = x.copy()
+    want_inter[0], want_inter[1] = -x[1], x[0]
+    want_inter[2], want_inter[3] = -x[2], -x[3]
+    return np.allclose(neox, want_neox, atol=1e-15) and np.allclose(inter, want_inter, atol=1e-15)
+
+
+def pin_rotation_properties(mod):
+    """Norm kept; <R_m q, R_n k> depends on m - n only; position 0 is the
+    identity -- for both pairings."""
+    rng = np.random.default_rng(0)
+    cs = roformer_cache(64)
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    ok = True
+    for neox in (True, False):
+        r = lambda v, p: mod.rotate(v, cs[p, :32], cs[p, 32:], neox)  # noqa: E731
+        ok &= abs(np.linalg.norm(r(q, 17)) - np.linalg.norm(q)) < 1e-12
+        ok &= np.allclose(r(q, 0), q, atol=0)
+        ok &= abs(r(q, 40) @ r(k, 33) - r(q, 7) @ r(k, 0)) < 1e-10
+        ok &= abs(r(q, 40) @ r(k, 33) - q @ k) > 1e-6  # and it does rotate
+    return bool(ok)
+
+
+def pin_pairings_differ_by_permutation(mod):
+    """Interleaved rotation = half rotation conjugated by the even/odd
+    permutation."""
+    rng = np.random.default_rng(1)
+    cs = roformer_cache(8)
+    x = rng.standard_normal(64)
+    perm = np.concatenate([np.arange(0, 64, 2), np.arange(1, 64, 2)])  # interleaved -> halves
+    a = mod.rotate(x, cs[5, :32], cs[5, 32:], False)
+    b = mod.rotate(x[perm], cs[5, :32], cs[5, 32:], True)
+    return np.allclose(a[perm], b, atol=1e-15)
+
+
+def pin_e4m3_rounding(mod):
+    """Every code's value maps to itself; midpoints go to the even code;
+    just off a midpoint goes to the nearer; saturation at 448; sign kept."""
+    vals = O.decode_e4m3fn(np.arange(0x7F, dtype=np.uint8))
+    if not np.array_equal(mod.quantize_e4m3(vals), np.arange(0x7F, dtype=np.uint8)):
+        return False
+    mids = (vals[:-1] + vals[1:]) / 2
+    lo = np.arange(0x7E)
+    want = np.where(lo % 2 == 0, lo, lo + 1).astype(np.uint8)
+    if not np.array_equal(mod.quantize_e4m3(mids), want):
+        return False
+    eps = 1e-9
+    if not np.array_equal(mod.quantize_e4m3(mids * (1 + eps)), (lo + 1).astype(np.uint8)):
+        return False
+    if not np.array_equal(mod.quantize_e4m3(mids * (1 - eps)), lo.astype(np.uint8)):
+        return False
+    big = mod.quantize_e4m3(np.array([448.0, 449.0, 1e6, -1e6, -0.0, -1e-9]))
+    return np.array_equal(big, [0x7E, 0x7E, 0x7E, 0xFE, 0x80, 0x80])
+
+
+def pin_against_torch(mod):
+    """Values in range: the same codes as torch's float8_e4m3fn cast."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(2)
+    x = np.concatenate([rng.standard_normal(20000) * s for s in (0.01, 1.0, 30.0)])
+    x = x[np.abs(x) < 440]
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    # float32 first (torch's input); exact values here, as e4m3 midpoints are float32-exact
+    return np.array_equal(mod.quantize_e4m3(x.astype(np.float32).astype(np.float64)), want)
+
+
+def pin_cache_write_round_trip(mod):
+    """Rows written at slots come back through the decode oracle's gather in
+    token order; other rows are unchanged."""
+    rng = np.random.default_rng(3)
+    page = 32
+    kv = rng.integers(0, 65535, size=(6, page, 576), dtype=np.uint16)
+    bt = np.array([4, 1, 5], dtype=np.int64)
+    slots = np.array([bt[j // page] * page + j % page for j in range(70)])
+    rows = rng.integers(0, 65535, size=(70, 576), dtype=np.uint16)
+    new = mod.kv_cache_write(kv, rows, slots, page)
+    back = O.gather_rows(new, bt, 70, page)
+    untouched = np.ones((6, page), dtype=bool)
+    untouched[slots // page, slots % page] = False
+    return np.array_equal(back, rows) and np.array_equal(new[untouched], kv[untouched])
+
+
+def all_pins(mod):
+    return [pin_hand_rotation(mod), pin_rotation_properties(mod), pin_pairings_differ_by_permutation(mod),
+            pin_e4m3_rounding(mod), pin_against_torch(mod), pin_cache_write_round_trip(mod)]
+
+
+def test_hand_rotation():
+    assert pin_hand_rotation(K)
+
+
+def test_rotation_properties():
+    assert pin_rotation_properties(K)
+
+
+def test_pairings_related_by_permutation():
+    assert pin_pairings_differ_by_permutation(K)
+
+
+def test_e4m3_rounding():
+    assert pin_e4m3_rounding(K)
+
+
+def test_e4m3_against_torch():
+    assert pin_against_torch(K)
+
+
+def test_cache_write_round_trip():
+    assert pin_cache_write_round_trip(K)
+
+
+def test_rope_quantize_shapes_and_values():
+    """The fused oracle is the composition of its parts."""
+    rng = np.random.default_rng(4)
+    from paged_mla_decode_08_gb300 import workloads as W
+    t, h = 3, 2
+    qn = W.f32_to_bf16_bits(rng.standard_normal((t, h, 512), dtype=np.float32))
+    qr = W.f32_to_bf16_bits(rng.standard_normal((t, h, 64), dtype=np.float32))
+    kn = W.f32_to_bf16_bits(rng.standard_normal((t, 512), dtype=np.float32))
+    kr = W.f32_to_bf16_bits(rng.standard_normal((t, 64), dtype=np.float32))
+    cs = roformer_cache(100)
+    pos = np.array([0, 7, 99])
+    qc, kc, qv, kv = K.rope_quantize_fp8(qn, qr, kn, kr, pos, cs, False)
+    assert qc.shape == (t, h, 576) and kc.shape == (t, 576)
+    assert np.array_equal(qv[0, :, 512:], O.decode_bf16(qr[0]))          # position 0: identity
+    assert np.array_equal(kc[:, :512], K.quantize_e4m3(O.decode_bf16(kn)))
+    r = K.rotate(O.decode_bf16(kr[2]), cs[99, :32], cs[99, 32:], False)
+    assert np.array_equal(kc[2, 512:], K.quantize_e4m3(r))
+    assert math.isclose(np.linalg.norm(kv[1, 512:]), np.linalg.norm(O.decode_bf16(kr[1])), rel_tol=1e-12)
+
+
+MUTATIONS = [
+    ("sine sign swapped",
+     "        out[..., :half] = a * cos - b * sin\n        out[..., half:] = b * cos + a * sin",
+     "        out[..., :half] = a * cos + b * sin\n        out[..., half:] = b * cos - a * sin"),
+    ("pairings swapped",
+     "    if is_neox:\n        a, b = x[..., :half], x[..., half:]",
+     "    if not is_neox:\n        a, b = x[..., :half], x[..., half:]"),
+    ("interleaved pairs off by one",
+     "        a, b = x[..., 0::2], x[..., 1::2]\n        out[..., 0::2]",
+     "        a, b = x[..., 1::2], x[..., 0::2]\n        out[..., 0::2]"),
+    ("truncation instead of rounding",
+     "    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))",
+     "    pick_hi = np.zeros(np.shape(d_hi), dtype=bool)"),
+    ("ties away from zero",
+     "((d_hi == d_lo) & (hi % 2 == 0))", "(d_hi == d_lo)"),
+    ("sign dropped",
+     "    return (code | (neg.astype(np.uint8) << 7)).astype(np.uint8)", "    return code"),
+    ("slot split by the wrong page size",
+     "        kv[slot // page_size, slot % page_size] = rows[t]", "        kv[slot // 64, slot % 64] = rows[t]"),
+]
+
+
+def mutated(old, new):
+    src = inspect.getsource(K).replace("from .mla_ref import", "from oracle.mla_ref import")
+    assert src.count(old) == 1, old
+    mod = types.ModuleType("kv_write_mutant")
+    exec(compile(src.replace(old, new), "kv_write_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(name, old, new):
+    try:
+        results = all_pins(mutated(old, new))
+    except (IndexError, ValueError):
+        return
+    assert not all(results), f"no pin rejects: {name}"
+
+
+def test_unmutated_passes_all_pins():
+    assert all(all_pins(K))
