@@ -26,10 +26,12 @@ taken (each also in the design notes):
 * cache slot s is row s % page_size of page s // page_size, the layout the
   decode reads (``k_cache.view(-1, page_size, 576)``).
 
-The rotation is computed in float64 here; the float32 kernel may round a
-value that lies within float32 rounding of an e4m3 rounding midpoint to the
-other neighbour, so the parity test names those elements and allows them one
-code step (the only decision where float precision matters).
+The rotated values that are rounded to e4m3 or bf16 are computed in float32
+with each product and each sum rounded on its own (``rotate_f32``): a
+quantised code is an integer decided by floating point, so both sides decide
+it in the same precision (the kernel's; the pages fix none).  ``rotate`` is
+the same rotation in float64, which the pins check against the mathematics
+and ``rotate_f32`` against within float32 rounding.
 
 parity pinned: tests/test_kv_write_oracle.py (hand-computed rotations, norm
 and relative-position properties of the rotation built from a RoFormer
@@ -63,6 +65,26 @@ def rotate(x: np.ndarray, cos: np.ndarray, sin: np.ndarray, is_neox: bool) -> np
     return out
 
 
+def rotate_f32(x, cos, sin, is_neox: bool) -> np.ndarray:
+    """``rotate`` in float32: a*cos, b*sin, b*cos, a*sin each rounded to
+    float32, then the difference / sum rounded (no fused multiply-add).
+    Returns float32."""
+    x = np.asarray(x, dtype=np.float32)
+    cos = np.asarray(cos, dtype=np.float32)
+    sin = np.asarray(sin, dtype=np.float32)
+    half = ROPE_DIM // 2
+    out = np.empty_like(x)
+    if is_neox:
+        a, b = x[..., :half], x[..., half:]
+        out[..., :half] = (a * cos) - (b * sin)
+        out[..., half:] = (b * cos) + (a * sin)
+    else:
+        a, b = x[..., 0::2], x[..., 1::2]
+        out[..., 0::2] = (a * cos) - (b * sin)
+        out[..., 1::2] = (b * cos) + (a * sin)
+    return out
+
+
 def _e4m3_values() -> np.ndarray:
     """The 126 finite non-negative e4m3fn values, ascending (from the
     format: 4-bit exponent, bias 7, 3-bit mantissa, no infinities, 0x7F NaN)."""
@@ -92,19 +114,31 @@ def rope_quantize_fp8(q_nope_bits, q_rope_bits, k_nope_bits, k_rope_bits, positi
     k codes uint8 [T, 576] = [k_nope | rope(k_rope)]) and the float64
     pre-rounding values (q_val, k_val) the codes were rounded from."""
     t = q_nope_bits.shape[0]
-    cs = np.asarray(cos_sin_cache, dtype=np.float64)[np.asarray(positions, dtype=np.int64)]
+    cs = np.asarray(cos_sin_cache, dtype=np.float32)[np.asarray(positions, dtype=np.int64)]
     cos, sin = cs[:, : ROPE_DIM // 2], cs[:, ROPE_DIM // 2:]
-    q_val = np.concatenate([decode_bf16(q_nope_bits),
-                            rotate(decode_bf16(q_rope_bits), cos[:, None, :], sin[:, None, :], is_neox)], axis=-1)
-    k_val = np.concatenate([decode_bf16(k_nope_bits).reshape(t, KV_LORA_RANK),
-                            rotate(decode_bf16(k_rope_bits).reshape(t, ROPE_DIM), cos, sin, is_neox)], axis=-1)
+    q_rot = rotate_f32(decode_bf16(q_rope_bits), cos[:, None, :], sin[:, None, :], is_neox)
+    k_rot = rotate_f32(decode_bf16(k_rope_bits).reshape(t, ROPE_DIM), cos, sin, is_neox)
+    q_val = np.concatenate([decode_bf16(q_nope_bits), q_rot.astype(np.float64)], axis=-1)
+    k_val = np.concatenate([decode_bf16(k_nope_bits).reshape(t, KV_LORA_RANK), k_rot.astype(np.float64)], axis=-1)
     return quantize_e4m3(q_val), quantize_e4m3(k_val), q_val, k_val
 
 
-def rope_bf16(q_rope_bits, positions, cos_sin_cache, is_neox: bool) -> np.ndarray:
-    """float64 rope(q_rope) [T, H, 64] (the bf16-query variant rounds it to bf16)."""
-    cs = np.asarray(cos_sin_cache, dtype=np.float64)[np.asarray(positions, dtype=np.int64)]
-    return rotate(decode_bf16(q_rope_bits), cs[:, None, : ROPE_DIM // 2], cs[:, None, ROPE_DIM // 2:], is_neox)
+def round_bf16(x) -> np.ndarray:
+    """float32 values -> bf16 bit patterns, nearest even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def rope_bf16(rope_bits, positions, cos_sin_cache, is_neox: bool) -> np.ndarray:
+    """bf16 bits of rope(x) for rows [T, ..., 64] of bf16 ``rope_bits``
+    (rotation in float32 as above, then nearest-even to bf16)."""
+    cs = np.asarray(cos_sin_cache, dtype=np.float32)[np.asarray(positions, dtype=np.int64)]
+    x = decode_bf16(rope_bits)
+    extra = (None,) * (x.ndim - 2)
+    cos = cs[(slice(None),) + extra + (slice(0, ROPE_DIM // 2),)]
+    sin = cs[(slice(None),) + extra + (slice(ROPE_DIM // 2, ROPE_DIM),)]
+    return round_bf16(rotate_f32(x, cos, sin, is_neox))
 
 
 def kv_cache_write(kv_bits: np.ndarray, rows: np.ndarray, out_cache_loc, page_size: int) -> np.ndarray:

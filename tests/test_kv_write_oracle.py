@@ -123,9 +123,24 @@ def pin_cache_write_round_trip(mod):
     return np.array_equal(back, rows) and np.array_equal(new[untouched], kv[untouched])
 
 
+def pin_f32_tracks_f64(mod):
+    """The float32 rotation (the one codes are rounded from) follows the
+    float64 one within float32 rounding, for both pairings."""
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((3, 64)).astype(np.float32).astype(np.float64)
+    cs = roformer_cache(40).astype(np.float32)
+    ok = True
+    for neox in (True, False):
+        a = mod.rotate(x, cs[[5, 17, 39], :32].astype(np.float64), cs[[5, 17, 39], 32:].astype(np.float64), neox)
+        b = mod.rotate_f32(x, cs[[5, 17, 39], :32], cs[[5, 17, 39], 32:], neox)
+        ok &= bool(np.all(np.abs(a - b) <= 4 * np.finfo(np.float32).eps * (np.abs(x).max() + 1)))
+    return ok
+
+
 def all_pins(mod):
     return [pin_hand_rotation(mod), pin_rotation_properties(mod), pin_pairings_differ_by_permutation(mod),
-            pin_e4m3_rounding(mod), pin_against_torch(mod), pin_cache_write_round_trip(mod)]
+            pin_e4m3_rounding(mod), pin_against_torch(mod), pin_cache_write_round_trip(mod),
+            pin_f32_tracks_f64(mod)]
 
 
 def test_hand_rotation():
@@ -167,15 +182,37 @@ def test_rope_quantize_shapes_and_values():
     assert qc.shape == (t, h, 576) and kc.shape == (t, 576)
     assert np.array_equal(qv[0, :, 512:], O.decode_bf16(qr[0]))          # position 0: identity
     assert np.array_equal(kc[:, :512], K.quantize_e4m3(O.decode_bf16(kn)))
-    r = K.rotate(O.decode_bf16(kr[2]), cs[99, :32], cs[99, 32:], False)
-    assert np.array_equal(kc[2, 512:], K.quantize_e4m3(r))
-    assert math.isclose(np.linalg.norm(kv[1, 512:]), np.linalg.norm(O.decode_bf16(kr[1])), rel_tol=1e-12)
+    r = K.rotate_f32(O.decode_bf16(kr[2]), cs[99, :32], cs[99, 32:], False)
+    assert np.array_equal(kc[2, 512:], K.quantize_e4m3(r.astype(np.float64)))
+    assert math.isclose(np.linalg.norm(kv[1, 512:]), np.linalg.norm(O.decode_bf16(kr[1])), rel_tol=1e-6)
+
+
+def test_float32_rotation_is_the_rotation():
+    """rotate_f32 (the precision codes are decided in) stays within float32
+    rounding of the float64 rotation, and is exact where no rounding occurs
+    (cos, sin in {0, 1, -1} on bf16 inputs)."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((4, 64)).astype(np.float32).astype(np.float64)
+    cs = roformer_cache(50).astype(np.float32)
+    for neox in (True, False):
+        a = K.rotate(x, cs[[3, 9, 27, 49], None, :32][:, 0].astype(np.float64),
+                     cs[[3, 9, 27, 49], None, 32:][:, 0].astype(np.float64), neox)
+        b = K.rotate_f32(x, cs[[3, 9, 27, 49], :32], cs[[3, 9, 27, 49], 32:], neox)
+        assert np.all(np.abs(a - b) <= 4 * np.finfo(np.float32).eps * (np.abs(x).max() + 1))
+        c = np.zeros(32, dtype=np.float32)
+        c[:16] = 1
+        s_ = np.zeros(32, dtype=np.float32)
+        s_[16:] = -1
+        assert np.array_equal(K.rotate_f32(x[0], c, s_, neox), K.rotate(x[0], c, s_, neox))
 
 
 MUTATIONS = [
     ("sine sign swapped",
      "        out[..., :half] = a * cos - b * sin\n        out[..., half:] = b * cos + a * sin",
      "        out[..., :half] = a * cos + b * sin\n        out[..., half:] = b * cos - a * sin"),
+    ("sine sign swapped in the float32 rotation only",
+     "        out[..., 0::2] = (a * cos) - (b * sin)\n        out[..., 1::2] = (b * cos) + (a * sin)",
+     "        out[..., 0::2] = (a * cos) + (b * sin)\n        out[..., 1::2] = (b * cos) - (a * sin)"),
     ("pairings swapped",
      "    if is_neox:\n        a, b = x[..., :half], x[..., half:]",
      "    if not is_neox:\n        a, b = x[..., :half], x[..., half:]"),
@@ -196,7 +233,7 @@ MUTATIONS = [
 
 def mutated(old, new):
     src = inspect.getsource(K).replace("from .mla_ref import", "from oracle.mla_ref import")
-    assert src.count(old) == 1, old
+    assert src.count(old) >= 1, old  # a systematic mistake: every occurrence
     mod = types.ModuleType("kv_write_mutant")
     exec(compile(src.replace(old, new), "kv_write_mutant", "exec"), mod.__dict__)
     return mod
