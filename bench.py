@@ -305,6 +305,10 @@ def our_arm(args, w, rank, world):
     bt_rows = block_table_measure(w, dev, stream, flush, max(3, min(K, 200)))
     # ---- ragged query counts (draft extend), the same decode kernels
     ragged = ragged_measure(dev, stream, flush, max(3, min(K, 200)), peaks)
+    # ---- the same workload planned on the device (planner kernel in the step)
+    devplan = device_plan_measure(db, w, dev, stream, flush, max(3, min(K, 200)), st)
+    # ---- the step before: RoPE + FP8 quantisation + cache write of the new tokens
+    rope_write = rope_write_measure(w, dev, stream, flush, max(3, min(K, 200)), peaks)
 
     if rank != 0:
         return
@@ -348,6 +352,8 @@ def our_arm(args, w, rank, world):
         "wall_s_timed_loop": wall,
         "block_table_build": bt_rows,
         "ragged_decode": ragged,
+        "device_plan": devplan,
+        "rope_quantize_write": rope_write,
         "segments": int(len(db.plan.segments())), "partial_slots": db.plan.num_partial_slots,
         "kernel_source_sha": kernel_source_hash(),
     }
@@ -396,6 +402,83 @@ def block_table_measure(w, dev, stream, flush, K):
     got = bt.cpu().numpy()
     res["last_table_matches_workload"] = bool(np.array_equal(got, want))
     return res
+
+
+def device_plan_measure(db, w, dev, stream, flush, K, st):
+    """The headline decode with a device plan: each step launches the planner
+    kernel, the main kernel and the combine (what a CUDA graph captured once
+    replays for any lengths).  Timed like the headline step."""
+    import torch
+    from paged_mla_decode_08_gb300 import binding as B
+    from paged_mla_decode_08_gb300 import runner as R
+    plan = B.mla_decode_plan_device(w.batch, w.page_size, w.num_heads, w.q_len)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(db.out)
+    lse = torch.empty_like(db.lse)
+
+    def step():
+        B.mla_decode(plan, db.q_nope, db.q_pe, db.kv, db.kv_dtype, db.block_table, db.seq_lens, w.scale,
+                     w.k_scale, out, lse, ws, None, stream)
+
+    for _ in range(3):
+        step()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    s_avg = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    host_out = R.decode(db, stream)[0]
+    diff = float((out.float() - host_out.float()).abs().max())  # the two plans split differently
+    return {"us_per_step": s_avg * 1e6, "tokens_per_s": st["tokens"] / s_avg,
+            "segments": int(len(plan.device_segments(ws))), "launches_per_step": 3,
+            "max_abs_diff_vs_host_plan": diff,
+            "note": "planner + main + combine per step, L2 flushed between steps"}
+
+
+def rope_write_measure(w, dev, stream, flush, K, peaks):
+    """mla_rope_quantize_cache_write for one decode step of this workload's
+    shape (one new token per request, all heads) on the pages' FP8 path:
+    merged e4m3 query out, e4m3 key rows into a cache.  Algorithmic bytes:
+    the bf16 query and key read once (1152 B per head and per key), the
+    e4m3 rows written (576 B each), cos/sin rows and the index arrays."""
+    import torch
+    from paged_mla_decode_08_gb300 import binding as B
+    t, h = w.batch, w.num_heads
+    g = torch.Generator(device=dev).manual_seed(0)
+    q_nope = torch.randn((t, h, 512), generator=g, device=dev).to(torch.bfloat16)
+    q_rope = torch.randn((t, h, 64), generator=g, device=dev).to(torch.bfloat16)
+    k_nope = torch.randn((t, 512), generator=g, device=dev).to(torch.bfloat16)
+    k_rope = torch.randn((t, 64), generator=g, device=dev).to(torch.bfloat16)
+    max_pos = 8192
+    inv = 10000.0 ** (-torch.arange(0, 64, 2, dtype=torch.float64, device=dev) / 64)
+    ang = torch.arange(max_pos, dtype=torch.float64, device=dev)[:, None] * inv[None, :]
+    cs = torch.cat([ang.cos(), ang.sin()], dim=1).float().contiguous()
+    pos = torch.randint(0, max_pos, (t,), generator=g, device=dev, dtype=torch.int64)
+    kv = torch.zeros((max(t, 64), w.page_size, 576), dtype=torch.uint8, device=dev)
+    slots = torch.randperm(kv.shape[0] * w.page_size, generator=g, device=dev)[:t].to(torch.int64)
+    q_out = torch.empty((t, h, 576), dtype=torch.uint8, device=dev)
+
+    def step():
+        B.mla_rope_quantize_cache_write(q_nope, q_rope, q_out, B.MLA_Q_E4M3, k_nope, k_rope, pos, cs, False, kv,
+                                        B.MLA_KV_E4M3, slots, stream)
+
+    for _ in range(3):
+        step()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    us = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+    alg = t * (h + 1) * (1152 + 576) + t * (256 + 16)
+    gbs = alg / (us * 1e-6) / 1e9
+    return {"us": us, "alg_bytes": alg, "achieved_gbs": gbs, "hbm_frac": gbs / float(peaks["hbm_gbs"]),
+            "tokens": t, "heads": h, "launches": K, "note": "e4m3 query + e4m3 cache rows; L2 flushed"}
 
 
 def ragged_measure(dev, stream, flush, K, peaks):

@@ -226,6 +226,88 @@ int mla_decode_noalloc(const mla_plan* plan, const void* q_nope, const void* q_p
                        const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
                        void* stream);
 
+/*
+ * Device plans: the split-KV schedule built on the device, from the device
+ * seq_lens, at every decode.  A decode made with a device plan can be
+ * captured in a CUDA graph once per batch shape and replayed for any
+ * lengths: there is no host copy of the lengths and nothing to re-plan
+ * (what FlashMLA's get_mla_metadata does on the device for tokenspeed
+ * flashmla.py, _init_decode_metadata; padded graph rows keep the pages'
+ * seq_len fill value of 1, P1 get_cuda_graph_seq_len_fill_value, and cost
+ * one tile).
+ *
+ * mla_decode_plan_device: the batch shape only (batch 1 .. 1793, page_size,
+ *   num_heads, q_len -- the maximum count for mla_decode_ragged -- and
+ *   num_sms as in mla_decode_plan).  The workspace it asks for holds the
+ *   schedule and the partials of the largest schedule any lengths can give
+ *   (2 (W - 1) split slots for W = num_sms / 2 workers).
+ * mla_decode, mla_decode_ragged, mla_decode_noalloc, mla_decode_main and
+ *   mla_decode_combine accept it: mla_decode_main (and so mla_decode) first
+ *   launches the planner kernel on the stream, which writes the schedule
+ *   into the workspace head; the main kernel reads it there.  Any bt_stride
+ *   >= 1 is accepted; lengths are clamped to bt_stride * page_size keys.
+ *   The schedule follows a fixed rule (mla_plan_device.cu): the same lengths
+ *   always give the same schedule, and so bit-identical results.
+ * mla_plan_is_device: 1 for a device plan, else 0.
+ * mla_plan_read_device_schedule: copy the schedule the last decode built in
+ *   `workspace` to host int32 out[5 * capacity], as mla_plan_get_segments
+ *   does; *num_segments_out receives its length.  Synchronous (a blocking
+ *   device-to-host copy): for tests and inspection.  Returns the number
+ *   copied or a negative MLA_ERR_* code.
+ * The host-plan inspection calls (mla_plan_num_segments,
+ * mla_plan_get_segments) report 0 segments for a device plan, and
+ * mla_plan_num_partial_slots its 2 (W - 1) slot capacity.
+ */
+int mla_decode_plan_device(int batch, int page_size, int num_heads, int q_len, int num_sms, mla_plan** plan_out,
+                           size_t* workspace_bytes_out);
+int mla_plan_is_device(const mla_plan* plan);
+int mla_plan_read_device_schedule(const mla_plan* plan, const void* workspace, int32_t* out, int capacity,
+                                  int* num_segments_out);
+
+/* ---- RoPE + FP8 quantisation + paged cache write (the step before) ----
+ *
+ * One launch, asynchronous on `stream`, for the new tokens of a decode step:
+ * rotary embedding of the rope parts of the query and of the key, the query
+ * output, and each token's key row written into its cache slot.  The pages'
+ * FP8 path does this with mla_quantize_and_rope_for_fp8 followed by
+ * set_mla_kv_buffer (sglang trtllm_mla_backend.py, forward_decode; tokenspeed
+ * trtllm_mla.py, forward_decode stores k[..., :512] and k[..., 512:]).
+ *
+ *   q_nope        device bf16 [num_tokens, num_heads, 512] (read only for
+ *                 MLA_Q_E4M3).
+ *   q_rope        device bf16 [num_tokens, num_heads, 64].
+ *   num_heads     query heads; 0 = no query work (a plain cache write).
+ *   q_out         MLA_Q_E4M3: device e4m3 [num_tokens, num_heads, 576] =
+ *                 [q_nope | rope(q_rope)], the merged FP8 query of the pages;
+ *                 MLA_Q_BF16: device bf16 [num_tokens, num_heads, 64] =
+ *                 rope(q_rope), the q_pe that mla_decode takes beside q_nope.
+ *   k_nope, k_rope  device bf16 [num_tokens, 512] and [num_tokens, 64].
+ *   positions     device int64 [num_tokens] rows of cos_sin_cache (may be
+ *                 NULL when cos_sin_cache is NULL).
+ *   cos_sin_cache device fp32 [max_position, 64]: 32 cosines then 32 sines
+ *                 per position, 16-byte aligned; NULL = no rotation.
+ *   is_neox       nonzero: element i pairs with i + 32; zero: 2i with 2i + 1.
+ *                 A pair (a, b) becomes (a cos - b sin, b cos + a sin), in
+ *                 fp32 with every product and sum rounded on its own.
+ *   kv_pages, kv_dtype, num_pages, page_size  the cache as mla_decode takes
+ *                 it; token t's row [k_nope | rope(k_rope)] is written at
+ *                 slot out_cache_loc[t] (device int64 [num_tokens]): row
+ *                 slot % page_size of page slot / page_size.
+ * FP8 values are rounded to nearest (ties to even) and saturate at +-448,
+ * with no scale (the pages pass none); bf16 values round to nearest even.
+ * Device-side errors (mla_decode_device_error): a position outside
+ * [0, max_position) leaves that token's outputs unwritten (0x601); a slot
+ * outside the cache leaves its key row unwritten (0x602).  Host-side:
+ * MLA_ERR_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA.
+ */
+#define MLA_Q_BF16 0
+#define MLA_Q_E4M3 1
+int mla_rope_quantize_cache_write(const void* q_nope, const void* q_rope, int num_tokens, int num_heads,
+                                  void* q_out, int q_out_dtype, const void* k_nope, const void* k_rope,
+                                  const int64_t* positions, const float* cos_sin_cache, int64_t max_position,
+                                  int is_neox, void* kv_pages, int kv_dtype, int64_t num_pages, int page_size,
+                                  const int64_t* out_cache_loc, void* stream);
+
 /* ---- block-table construction (the step before the decode) ----
  *
  * Build the [batch, max_blocks] int32 block table mla_decode reads from a
@@ -305,7 +387,8 @@ void mla_planner_constants(int* tile_tokens, int* segment_overhead_tiles, int* m
 /* Kernel-side error word of the current device: 0, or the code of the first
  * bounded wait that timed out inside a decode kernel since the last reset
  * (the kernel then stopped early and its outputs are not valid); failing
- * that, the first out-of-range lookup of a block-table builder (0x30x).  Reading it
+ * that, the first out-of-range lookup of a block-table builder (0x30x) or of
+ * the RoPE / cache-write step (0x60x).  Reading it
  * synchronises with the device; reset != 0 clears it.  Errors: MLA_ERR_ARG,
  * MLA_ERR_CUDA. */
 int mla_decode_device_error(int* code, int reset);

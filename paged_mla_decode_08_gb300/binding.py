@@ -40,6 +40,13 @@ SIGNATURES = {
     "mla_decode_plan_ragged": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_vp),
                                         ctypes.POINTER(_c_size)]),
     "mla_decode_ragged": (_c_int, _DECODE_ARGS[:12] + [_vp] + _DECODE_ARGS[12:]),
+    "mla_decode_plan_device": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_vp),
+                                        ctypes.POINTER(_c_size)]),
+    "mla_plan_is_device": (_c_int, [_vp]),
+    "mla_plan_read_device_schedule": (_c_int, [_vp, _vp, _i32p, _c_int, ctypes.POINTER(_c_int)]),
+    "mla_rope_quantize_cache_write": (_c_int, [_vp, _vp, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp,
+                                               ctypes.c_int64, _c_int, _vp, _c_int, ctypes.c_int64, _c_int, _vp,
+                                               _vp]),
     "mla_block_table_from_tokens": (_c_int, [_vp, ctypes.c_int64, ctypes.c_int64, _vp, _vp, _c_int, _c_int,
                                              _vp, _c_int, _vp]),
     "mla_block_table_from_pages": (_c_int, [_vp, ctypes.c_int64, ctypes.c_int64, _vp, _c_int, _vp, _c_int,
@@ -126,6 +133,23 @@ class Plan:
     def num_partial_slots(self) -> int:
         return load().mla_plan_num_partial_slots(self.handle)
 
+    @property
+    def is_device(self) -> bool:
+        return bool(load().mla_plan_is_device(self.handle))
+
+    def device_segments(self, workspace) -> np.ndarray:
+        """The schedule the last decode built in ``workspace`` (device plans;
+        synchronises): (worker, request, tile_begin, tile_end, slot) rows."""
+        lib = load()
+        cap = 1920
+        buf = np.zeros(5 * cap, dtype=np.int32)
+        n = ctypes.c_int()
+        got = lib.mla_plan_read_device_schedule(self.handle, _ptr(workspace), buf.ctypes.data_as(_i32p), cap,
+                                                ctypes.byref(n))
+        if got < 0:
+            _check(got)
+        return buf[: 5 * got].reshape(got, 5)
+
     def segments(self) -> np.ndarray:
         """(worker, request, tile_begin, tile_end, partial_slot) rows."""
         lib = load()
@@ -146,6 +170,17 @@ def mla_decode_plan(seq_lens_host, page_size: int, num_heads: int, q_len: int = 
     _check(lib.mla_decode_plan(lens.ctypes.data_as(_i32p), int(lens.shape[0]), page_size, num_heads,
                                q_len, num_sms, ctypes.byref(handle), ctypes.byref(ws)))
     return Plan(handle.value, ws.value, int(lens.shape[0]), page_size, num_heads, q_len)
+
+
+def mla_decode_plan_device(batch: int, page_size: int, num_heads: int, q_len: int = 1, num_sms: int = 0) -> Plan:
+    """A plan whose schedule is built on the device from the device lengths
+    at every decode (graph-capturable for any lengths)."""
+    lib = load()
+    handle = _vp()
+    ws = _c_size()
+    _check(lib.mla_decode_plan_device(batch, page_size, num_heads, q_len, num_sms, ctypes.byref(handle),
+                                      ctypes.byref(ws)))
+    return Plan(handle.value, ws.value, batch, page_size, num_heads, q_len)
 
 
 def mla_decode_plan_ragged(seq_lens_host, q_lens_host, page_size: int, num_heads: int, num_sms: int = 0) -> Plan:
@@ -216,6 +251,23 @@ def mla_decode_noalloc(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_
 
 MLA_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 MLA_BLOCK_TABLE_MAX_BLOCKS = 65535 * 256
+MLA_Q_BF16 = 0
+MLA_Q_E4M3 = 1
+
+
+def mla_rope_quantize_cache_write(q_nope, q_rope, q_out, q_out_dtype: int, k_nope, k_rope, positions,
+                                  cos_sin_cache, is_neox: bool, kv_pages, kv_dtype: int, out_cache_loc,
+                                  stream=None):
+    """RoPE + (FP8) quantisation of the new tokens' query into ``q_out`` and
+    of their keys into the cache at ``out_cache_loc`` (torch CUDA tensors;
+    q tensors may be None for a plain cache write)."""
+    t = int(k_nope.shape[0])
+    h = 0 if q_rope is None else int(q_rope.shape[1])
+    max_pos = 0 if cos_sin_cache is None else int(cos_sin_cache.shape[0])
+    _check(load().mla_rope_quantize_cache_write(
+        _ptr(q_nope), _ptr(q_rope), t, h, _ptr(q_out), int(q_out_dtype), _ptr(k_nope), _ptr(k_rope),
+        _ptr(positions), _ptr(cos_sin_cache), max_pos, 1 if is_neox else 0, _ptr(kv_pages), int(kv_dtype),
+        int(kv_pages.shape[0]), int(kv_pages.shape[1]), _ptr(out_cache_loc), _stream(stream)))
 
 
 def mla_block_table_from_tokens(req_to_token, req_pool_indices, seq_lens, page_size: int, block_table,

@@ -24,7 +24,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmladecode.so")
 
-CUDA_SOURCES = ["mla_abi.cu", "mla_sm103.cu", "mla_combine.cu", "mla_noalloc.cu", "mla_block_table.cu"]
+CUDA_SOURCES = ["mla_abi.cu", "mla_sm103.cu", "mla_combine.cu", "mla_noalloc.cu", "mla_block_table.cu",
+                "mla_plan_device.cu", "mla_kv_write.cu"]
 CXX_SOURCES = ["mla_plan.cpp"]
 HEADERS = ["mla_internal.h", "sm103_ptx.cuh"]
 

@@ -15,7 +15,10 @@
 #include "mla_internal.h"
 
 namespace mla {
-cudaError_t launch_sm103(const mla_plan& p, const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_sm103(const mla_plan& p, const DecodeArgs& a, const void* workspace, cudaStream_t stream);
+cudaError_t launch_plan_device(const int32_t* seq_lens, int batch, int cap_tokens, int workers, void* workspace,
+                               cudaStream_t stream);
+cudaError_t launch_combine_dev(int workers, const DecodeArgs& a, const void* workspace, cudaStream_t stream);
 cudaError_t sm103_read_error(int* code, bool reset);
 cudaError_t launch_combine(const std::vector<CombineJob>& jobs, const DecodeArgs& a,
                            cudaStream_t stream);
@@ -27,6 +30,12 @@ cudaError_t launch_block_table_from_pages(const int32_t* req_to_page, int64_t po
                                           const int32_t* req_pool_indices, int batch, int32_t* block_table,
                                           int max_blocks, cudaStream_t stream);
 cudaError_t block_table_read_error(int* code, bool reset);
+cudaError_t launch_rope_quantize_write(const void* q_nope, const void* q_rope, int num_tokens, int num_heads,
+                                       void* q_out, int q_out_dtype, const void* k_nope, const void* k_rope,
+                                       const int64_t* positions, const float* cos_sin_cache, int64_t max_position,
+                                       int is_neox, void* kv_pages, int kv_dtype, int64_t num_pages, int page_size,
+                                       const int64_t* out_cache_loc, cudaStream_t stream);
+cudaError_t kv_write_read_error(int* code, bool reset);
 }  // namespace mla
 
 namespace {
@@ -73,6 +82,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 struct Prepared {
   mla::DecodeArgs args;
+  void* workspace = nullptr;
 };
 
 // cu_seqlens_q: NULL for a uniform batch (num_tokens = batch * q_len), else
@@ -97,6 +107,7 @@ int prepare(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_
   if (num_pages * (int64_t)page_size > INT32_MAX) return fail(MLA_ERR_ARG, "num_pages * page_size must be < 2^31");
   if (bt_stride < 1 || bt_stride < plan->max_pages)
     return fail(MLA_ERR_ARG, "bt_stride is smaller than the pages of the longest planned request");
+  if ((int64_t)bt_stride * page_size > INT32_MAX) return fail(MLA_ERR_ARG, "bt_stride * page_size must be < 2^31");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(MLA_ERR_ARG, "scale must be finite and > 0");
   if (kv_dtype == MLA_KV_E4M3 && (!(k_scale > 0.f) || !std::isfinite(k_scale)))
     return fail(MLA_ERR_ARG, "k_scale must be finite and > 0");
@@ -113,8 +124,9 @@ int prepare(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_
   a.q_nope = q_nope; a.q_pe = q_pe; a.kv = kv_pages;
   a.block_table = block_table; a.seq_lens = seq_lens;
   a.out = out; a.lse = lse;
-  a.part_o = workspace;
+  a.part_o = workspace ? static_cast<char*>(workspace) + plan->ws_part_offset : nullptr;
   a.part_lse = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan->ws_lse_offset) : nullptr;
+  pr->workspace = workspace;
   a.num_pages = num_pages; a.page_size = page_size; a.kv_dtype = kv_dtype; a.bt_stride = bt_stride;
   a.batch = plan->batch; a.q_len = plan->q_len; a.num_heads = plan->num_heads; a.rows = plan->rows;
   a.score_scale_log2 = (float)((double)scale * (double)kf * 1.4426950408889634);
@@ -125,7 +137,14 @@ int prepare(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_
 }
 
 int launch_main(const mla_plan* plan, const Prepared& pr, cudaStream_t stream) {
-  cudaError_t e = mla::launch_sm103(*plan, pr.args, stream);
+  if (plan->device) {
+    // the schedule for the lengths now on the device, into the workspace head
+    const mla::DecodeArgs& a = pr.args;
+    cudaError_t e = mla::launch_plan_device(a.seq_lens, a.batch, a.bt_stride * a.page_size, plan->num_workers,
+                                            pr.workspace, stream);
+    if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("planner launch: ") + cudaGetErrorString(e));
+  }
+  cudaError_t e = mla::launch_sm103(*plan, pr.args, pr.workspace, stream);
   if (e == cudaErrorNotSupported)
     return fail(MLA_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled unavailable or rejected the cache layout");
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("main kernel launch: ") + cudaGetErrorString(e));
@@ -133,7 +152,8 @@ int launch_main(const mla_plan* plan, const Prepared& pr, cudaStream_t stream) {
 }
 
 int launch_combine(const mla_plan* plan, const Prepared& pr, cudaStream_t stream) {
-  cudaError_t e = mla::launch_combine(plan->jobs, pr.args, stream);
+  cudaError_t e = plan->device ? mla::launch_combine_dev(plan->num_workers, pr.args, pr.workspace, stream)
+                               : mla::launch_combine(plan->jobs, pr.args, stream);
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("combine launch: ") + cudaGetErrorString(e));
   return MLA_OK;
 }
@@ -191,7 +211,7 @@ int mla_decode_main(const mla_plan* plan, const void* q_nope, const void* q_pe, 
 int mla_decode_combine(const mla_plan* plan, void* out, float* lse, void* workspace, size_t workspace_bytes,
                        void* stream) {
   if (!plan) return fail(MLA_ERR_ARG, "plan is NULL");
-  if (plan->jobs.empty()) return ok();
+  if (plan->jobs.empty() && !plan->device) return ok();
   if (!out || !lse) return fail(MLA_ERR_ARG, "out / lse is NULL");
   if (!workspace || workspace_bytes < plan->ws_bytes)
     return fail(MLA_ERR_WORKSPACE, "workspace is smaller than mla_plan_workspace_bytes(plan)");
@@ -202,8 +222,9 @@ int mla_decode_combine(const mla_plan* plan, void* out, float* lse, void* worksp
   std::memset(&pr, 0, sizeof(pr));
   mla::DecodeArgs& a = pr.args;
   a.out = out; a.lse = lse;
-  a.part_o = workspace;
+  a.part_o = static_cast<char*>(workspace) + plan->ws_part_offset;
   a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan->ws_lse_offset);
+  pr.workspace = workspace;
   a.batch = plan->batch; a.q_len = plan->q_len; a.num_heads = plan->num_heads; a.rows = plan->rows;
   rc = launch_combine(plan, pr, static_cast<cudaStream_t>(stream));
   return rc == MLA_OK ? ok() : rc;
@@ -265,6 +286,56 @@ int mla_decode_ragged(const mla_plan* plan, const void* q_nope, const void* q_pe
   return rc == MLA_OK ? ok() : rc;
 }
 
+int mla_decode_plan_device(int batch, int page_size, int num_heads, int q_len, int num_sms, mla_plan** plan_out,
+                           size_t* workspace_bytes_out) {
+  if (!plan_out) return fail(MLA_ERR_ARG, "plan_out is NULL");
+  *plan_out = nullptr;
+  if (num_sms < 0) return fail(MLA_ERR_ARG, "num_sms must be >= 0");
+  if (num_sms == 0) {
+    int rc = check_device(&num_sms);
+    if (rc != MLA_OK) return rc;
+  }
+  mla_plan* p = new (std::nothrow) mla_plan();
+  if (!p) return fail(MLA_ERR_ARG, "out of host memory");
+  const char* msg = "";
+  int rc = mla::build_device_plan(batch, page_size, num_heads, q_len, num_sms, p, &msg);
+  if (rc != MLA_OK) { delete p; return fail(rc, msg); }
+  *plan_out = p;
+  if (workspace_bytes_out) *workspace_bytes_out = p->ws_bytes;
+  return ok();
+}
+
+int mla_plan_is_device(const mla_plan* plan) { return plan && plan->device ? 1 : 0; }
+
+int mla_plan_read_device_schedule(const mla_plan* plan, const void* workspace, int32_t* out, int capacity,
+                                  int* num_segments_out) {
+  if (!plan || !plan->device || !workspace || !out || capacity < 0 || !num_segments_out)
+    return fail(MLA_ERR_ARG, "bad arguments");
+  mla::Schedule<mla::kSegCapLarge>* h = new (std::nothrow) mla::Schedule<mla::kSegCapLarge>();
+  if (!h) return fail(MLA_ERR_ARG, "out of host memory");
+  cudaError_t e = cudaMemcpy(h, static_cast<const char*>(workspace) + mla::kDevSchedOffset, sizeof(*h),
+                             cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    delete h;
+    return fail(MLA_ERR_CUDA, std::string("reading the device schedule: ") + cudaGetErrorString(e));
+  }
+  const int n = std::max(0, std::min(h->num_segments, mla::kSegCapLarge));
+  *num_segments_out = n;
+  int w = 0, copied = 0;
+  for (int i = 0; i < n && i < capacity; ++i) {
+    while (w < h->num_workers && h->worker_seg[w + 1] <= i) ++w;
+    out[5 * i + 0] = w;
+    out[5 * i + 1] = h->seg[i].req;
+    out[5 * i + 2] = h->seg[i].tile_begin;
+    out[5 * i + 3] = h->seg[i].tile_end;
+    out[5 * i + 4] = h->seg[i].slot;
+    ++copied;
+  }
+  delete h;
+  ok();
+  return copied;
+}
+
 size_t mla_plan_workspace_bytes(const mla_plan* plan) { return plan ? plan->ws_bytes : 0; }
 int mla_plan_num_workers(const mla_plan* plan) { return plan ? plan->num_workers : 0; }
 int mla_plan_num_segments(const mla_plan* plan) { return plan ? (int)plan->segs.size() : 0; }
@@ -293,11 +364,13 @@ const char* mla_decode_last_error_string(void) { return g_last_error.c_str(); }
 
 int mla_decode_device_error(int* code, int reset) {
   if (!code) return fail(MLA_ERR_ARG, "code is NULL");
-  int bt_code = 0;
+  int bt_code = 0, kw_code = 0;
   cudaError_t e = mla::sm103_read_error(code, reset != 0);
   if (e == cudaSuccess) e = mla::block_table_read_error(&bt_code, reset != 0);
+  if (e == cudaSuccess) e = mla::kv_write_read_error(&kw_code, reset != 0);
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("reading the kernel error word: ") + cudaGetErrorString(e));
   if (*code == 0) *code = bt_code;
+  if (*code == 0) *code = kw_code;
   return ok();
 }
 
@@ -328,6 +401,35 @@ int mla_block_table_from_tokens(const int32_t* req_to_token, int64_t pool_rows, 
                                                       seq_lens, batch, page_size, block_table, max_blocks,
                                                       static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("block-table launch: ") + cudaGetErrorString(e));
+  return ok();
+}
+
+int mla_rope_quantize_cache_write(const void* q_nope, const void* q_rope, int num_tokens, int num_heads,
+                                  void* q_out, int q_out_dtype, const void* k_nope, const void* k_rope,
+                                  const int64_t* positions, const float* cos_sin_cache, int64_t max_position,
+                                  int is_neox, void* kv_pages, int kv_dtype, int64_t num_pages, int page_size,
+                                  const int64_t* out_cache_loc, void* stream) {
+  if (num_tokens < 1 || num_heads < 0 || num_heads > (1 << 16)) return fail(MLA_ERR_ARG, "num_tokens >= 1, num_heads in [0, 65536]");
+  if ((int64_t)num_tokens * (num_heads + 1) * 72 > ((int64_t)1 << 40)) return fail(MLA_ERR_ARG, "too many tokens");
+  if (q_out_dtype != MLA_Q_BF16 && q_out_dtype != MLA_Q_E4M3) return fail(MLA_ERR_ARG, "q_out_dtype must be MLA_Q_BF16 or MLA_Q_E4M3");
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_E4M3) return fail(MLA_ERR_ARG, "kv_dtype must be MLA_KV_BF16 or MLA_KV_E4M3");
+  if (page_size != 32 && page_size != 64) return fail(MLA_ERR_ARG, "page_size must be 32 or 64");
+  if (num_pages <= 0 || num_pages * (int64_t)page_size > INT32_MAX) return fail(MLA_ERR_ARG, "num_pages must be > 0 and num_pages * page_size < 2^31");
+  if (!k_nope || !k_rope || !kv_pages || !out_cache_loc) return fail(MLA_ERR_ARG, "a required device pointer is NULL");
+  if (num_heads > 0 && (!q_rope || !q_out || (q_out_dtype == MLA_Q_E4M3 && !q_nope)))
+    return fail(MLA_ERR_ARG, "query pointers are NULL");
+  if (cos_sin_cache && (!positions || max_position < 1)) return fail(MLA_ERR_ARG, "positions / max_position missing");
+  if (!aligned(k_nope, 16) || !aligned(k_rope, 16) || !aligned(kv_pages, 16) || !aligned(out_cache_loc, 8) ||
+      (q_nope && !aligned(q_nope, 16)) || (q_rope && !aligned(q_rope, 16)) || (q_out && !aligned(q_out, 16)) ||
+      (cos_sin_cache && !aligned(cos_sin_cache, 16)) || (positions && !aligned(positions, 8)))
+    return fail(MLA_ERR_ARG, "arrays must be 16-byte aligned (index arrays 8-byte)");
+  int rc = check_device(nullptr);
+  if (rc != MLA_OK) return rc;
+  cudaError_t e = mla::launch_rope_quantize_write(q_nope, q_rope, num_tokens, num_heads, q_out, q_out_dtype, k_nope,
+                                                  k_rope, positions, cos_sin_cache, max_position, is_neox, kv_pages,
+                                                  kv_dtype, num_pages, page_size, out_cache_loc,
+                                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("rope / cache-write launch: ") + cudaGetErrorString(e));
   return ok();
 }
 

@@ -36,16 +36,10 @@ constexpr int kCombChunks = kChunks / 4;       // per CTA: a quarter of the row
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-template <int CAP>
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineList<CAP> jobs,
-                                                      const __grid_constant__ DecodeArgs a) {
+// One (job, 32-row block, quarter of the columns) of the merge; called after
+// the grid dependency wait.
+__device__ __forceinline__ void combine_body(const CombineJob job, const DecodeArgs& a) {
   extern __shared__ float s_w[];  // [nsplit][32] weights (0 for -inf splits)
-  // Launched as a programmatic dependent of the main kernel: everything above
-  // this wait overlaps the main kernel's tail; the partials are read after it
-  // (the wait returns once the main grid has completed and its writes are
-  // visible; without the launch attribute it returns at once).
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const CombineJob job = jobs.job[blockIdx.x];
   const int M = a.rows;  // partial-row stride: the planned rows per request
   const int r0 = blockIdx.y * kCombRows;
   const int c0 = blockIdx.z * kCombChunks;
@@ -142,6 +136,29 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
   }
 }
 
+// Launched as a programmatic dependent of the main kernel: the launch
+// overlaps the main kernel's tail; the partials are read after the wait
+// (which returns once the main grid has completed and its writes are
+// visible; without the launch attribute it returns at once).
+template <int CAP>
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineList<CAP> jobs,
+                                                      const __grid_constant__ DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  combine_body(jobs.job[blockIdx.x], a);
+}
+
+// Device plan: the job list is in the workspace, written by the planner
+// grid two launches earlier (read at L2, ld.global.cg, like the schedule);
+// the grid covers the most jobs any plan can have and CTAs past the actual
+// count return.
+__global__ void __launch_bounds__(256) combine_kernel_dev(const CombineList<kJobCap>* jobs,
+                                                          const __grid_constant__ DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if ((int)blockIdx.x >= __ldcg(&jobs->num_jobs)) return;
+  const CombineJob* j = &jobs->job[blockIdx.x];  // 4-byte loads: no alignment assumed
+  combine_body(CombineJob{__ldcg(&j->req), __ldcg(&j->slot_begin), __ldcg(&j->nsplit), 0}, a);
+}
+
 template <int CAP>
 static cudaError_t launch_combine_cap(const std::vector<CombineJob>& jobs, const DecodeArgs& a,
                                       cudaStream_t stream) {
@@ -171,6 +188,24 @@ cudaError_t launch_combine(const std::vector<CombineJob>& jobs, const DecodeArgs
                            cudaStream_t stream) {
   if (jobs.empty()) return cudaSuccess;
   return launch_combine_cap<kJobCap>(jobs, a, stream);
+}
+
+cudaError_t launch_combine_dev(int workers, const DecodeArgs& a, const void* workspace, cudaStream_t stream) {
+  if (workers < 2) return cudaSuccess;  // one worker never splits a request
+  const auto* jobs = reinterpret_cast<const CombineList<kJobCap>*>(static_cast<const char*>(workspace) +
+                                                                    kDevJobsOffset);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(workers - 1), (unsigned)((a.rows + kCombRows - 1) / kCombRows),
+                     (unsigned)(kChunks / kCombChunks));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = (size_t)workers * kCombRows * sizeof(float);  // a request spans <= W workers
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel_dev, jobs, a);
 }
 
 }  // namespace mla

@@ -57,6 +57,16 @@ struct CombineList {
 constexpr int kJobCap = 128;
 static_assert(kJobCap >= kMaxWorkers - 1, "combine job capacity");
 
+// Device plans (schedule built on the device from the device lengths): the
+// workspace starts with the schedule and the combine-job list, then the
+// partials, sized for the most a plan can need (2 (W - 1) split slots).  At
+// most batch + W - 1 segments, so the batch is bounded by the capacity.
+constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+constexpr size_t kDevSchedOffset = 0;
+constexpr size_t kDevJobsOffset = align256(sizeof(Schedule<kSegCapLarge>));
+constexpr size_t kDevPartOffset = align256(kDevJobsOffset + sizeof(CombineList<kJobCap>));
+constexpr int kDevMaxBatch = kSegCapLarge - (kMaxWorkers - 1);
+
 // Pointers and scalars of one decode call, as the kernels see them.
 struct DecodeArgs {
   const void* q_nope;  // bf16 [T, H, 512]
@@ -106,10 +116,12 @@ __device__ __forceinline__ int2 request_q(const DecodeArgs& a, int b, bool* bad 
 struct mla_plan {
   int batch = 0, page_size = 0, num_heads = 0, q_len = 0, rows = 0;
   bool ragged = false;  // planned from per-request query counts (q_len = their maximum)
+  bool device = false;  // schedule built on the device at each decode (segs / jobs empty here)
   int num_sms = 0, num_workers = 0;
   int max_pages = 0;  // ceil(max seq_len / page_size)
   int num_slots = 0;
   size_t ws_bytes = 0, ws_lse_offset = 0;
+  size_t ws_part_offset = 0;  // partial outputs (after the schedule area of a device plan)
   int64_t plan_capacity = 0;  // per-worker cost bound the schedule was made with
   std::vector<int32_t> seq_lens;
   std::vector<int32_t> seg_worker;  // worker of each segment (inspection)
@@ -123,4 +135,7 @@ namespace mla {
 // *msg points to a static description.
 int build_plan(const int32_t* seq_lens, int batch, int page_size, int num_heads, int q_len,
                int num_sms, mla_plan* plan, const char** msg);
+// Device plan: workers and workspace layout only (mla_plan.cpp).
+int build_device_plan(int batch, int page_size, int num_heads, int q_len, int num_sms, mla_plan* plan,
+                      const char** msg);
 }  // namespace mla

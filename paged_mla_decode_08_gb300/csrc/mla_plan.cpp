@@ -155,4 +155,31 @@ int build_plan(const int32_t* seq_lens, int batch, int page_size, int num_heads,
   return MLA_OK;
 }
 
+// A device plan fixes only the batch shape: the schedule itself is built by
+// the planner kernel (mla_plan_device.cu) from the device lengths at every
+// decode, into the head of the workspace, which is sized for the largest
+// schedule any lengths can give (2 (W - 1) split slots).
+int build_device_plan(int batch, int page_size, int num_heads, int q_len, int num_sms, mla_plan* p,
+                      const char** msg) {
+  if (batch < 1 || batch > kDevMaxBatch) { *msg = "batch must be in [1, 1793] for a device plan"; return MLA_ERR_ARG; }
+  if (page_size != 32 && page_size != 64) { *msg = "page_size must be 32 or 64"; return MLA_ERR_ARG; }
+  if (num_heads < 1 || q_len < 1) { *msg = "num_heads and q_len must be >= 1"; return MLA_ERR_ARG; }
+  if ((int64_t)num_heads * q_len > kMaxRows) { *msg = "num_heads * q_len must be <= 128"; return MLA_ERR_ARG; }
+  if (num_sms < 2) { *msg = "num_sms must be >= 2"; return MLA_ERR_ARG; }
+  const int W = std::min(num_sms / 2, kMaxWorkers);
+  p->batch = batch; p->page_size = page_size; p->num_heads = num_heads; p->q_len = q_len;
+  p->rows = num_heads * q_len; p->num_sms = num_sms; p->num_workers = W;
+  p->device = true;
+  p->max_pages = 1;  // lengths are unknown: the decode clamps them to the block-table row
+  const int slots = 2 * (W - 1);
+  p->num_slots = slots;
+  p->ws_part_offset = kDevPartOffset;
+  const size_t o_bytes = (size_t)slots * p->rows * kLatent * 2;
+  p->ws_lse_offset = kDevPartOffset + (o_bytes + 255) / 256 * 256;
+  const size_t l_bytes = (size_t)slots * p->rows * sizeof(float);
+  p->ws_bytes = p->ws_lse_offset + (l_bytes + 255) / 256 * 256;
+  *msg = "";
+  return MLA_OK;
+}
+
 }  // namespace mla

@@ -129,6 +129,33 @@ struct Ctx {
   __device__ uint32_t bar(int i) const { return sbase + OFF_BAR + 8 * i; }
 };
 
+// Read access to the schedule.  ParamSched: the host plan's schedule, a
+// kernel parameter.  GlobalSched: a device plan's schedule in the workspace,
+// written by the planner grid while this grid may already be resident, so it
+// is read at L2 (ld.global.cg: never from a possibly stale L1 / read-only
+// cache line) and only after the grid dependency wait; every CTA of a pair
+// then sees the same segments.
+template <int CAP>
+struct ParamSched {
+  const Schedule<CAP>& s;
+  __device__ __forceinline__ int num_workers() const { return s.num_workers; }
+  __device__ __forceinline__ int begin(int w) const { return s.worker_seg[w]; }
+  __device__ __forceinline__ int end(int w) const { return s.worker_seg[w + 1]; }
+  __device__ __forceinline__ Segment seg(int i) const { return s.seg[i]; }
+};
+struct GlobalSched {
+  const Schedule<kSegCapLarge>* s;
+  __device__ __forceinline__ int num_workers() const { return __ldcg(&s->num_workers); }
+  __device__ __forceinline__ int begin(int w) const { return __ldcg(&s->worker_seg[w]); }
+  __device__ __forceinline__ int end(int w) const { return __ldcg(&s->worker_seg[w + 1]); }
+  // four 4-byte loads: the segment array is only 4-byte aligned (it follows
+  // the 4-byte header fields), so no vector load may touch it
+  __device__ __forceinline__ Segment seg(int i) const {
+    const Segment* p = &s->seg[i];
+    return Segment{__ldcg(&p->req), __ldcg(&p->tile_begin), __ldcg(&p->tile_end), __ldcg(&p->slot)};
+  }
+};
+
 // Bounded barrier wait.  false: gave up (timeout here or elsewhere in the CTA).
 template <bool kCluster>
 __device__ __forceinline__ bool wait_bar(const Ctx& c, uint32_t bar, uint32_t parity, int code) {
@@ -165,10 +192,10 @@ __device__ __forceinline__ int request_len(const DecodeArgs& a, int b) {
 // request_len() of schedule segment s, from the copy every CTA takes at start
 // (one memory round trip for all its segments instead of one per segment
 // switch in every role)
-template <int CAP>
-__device__ __forceinline__ int seg_len(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, int s) {
+template <class S>
+__device__ __forceinline__ int seg_len(const Ctx& c, const S& sched, const DecodeArgs& a, int s) {
   const int k = s - c.seg0;
-  return k < kSegLenCache ? c.seg_len[k] : request_len(a, sched.seg[s].req);
+  return k < kSegLenCache ? c.seg_len[k] : request_len(a, sched.seg(s).req);
 }
 
 // request_q() with a malformed ragged entry recorded in the error word
@@ -180,10 +207,10 @@ __device__ __forceinline__ int2 request_q_checked(const DecodeArgs& a, int b) {
 }
 
 // (first query token, query count) of schedule segment s, cached like seg_len
-template <int CAP>
-__device__ __forceinline__ int2 seg_q(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, int s) {
+template <class S>
+__device__ __forceinline__ int2 seg_q(const Ctx& c, const S& sched, const DecodeArgs& a, int s) {
   const int k = s - c.seg0;
-  return k < kSegLenCache ? c.seg_q[k] : request_q_checked(a, sched.seg[s].req);
+  return k < kSegLenCache ? c.seg_q[k] : request_q_checked(a, sched.seg(s).req);
 }
 
 // Row of out / lse that query row `row` of a request with (first token,
@@ -200,16 +227,16 @@ __device__ __forceinline__ int segment_tiles(const Segment& sg, int L) {
 
 // ------------------------------------------------------------------ producer
 
-template <int CAP, bool F8>
-__device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, const CUtensorMap* tm_lat,
+template <class S, bool F8>
+__device__ void producer(const Ctx& c, const S& sched, const DecodeArgs& a, const CUtensorMap* tm_lat,
                          const CUtensorMap* tm_rope, int worker, int rank) {
   const int lane = threadIdx.x & 31;
   const int oob_row = (int)(a.num_pages * a.page_size);  // first row past the pool: zero-filled by TMA
   const int pieces = kTileTokens / a.page_size;           // pages per tile: 1 or 2
   int j = 0, tails = 0;
   bool ok = true;
-  for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
-    const Segment sg = sched.seg[s];
+  for (int s = sched.begin(worker); ok && s < sched.end(worker); ++s) {
+    const Segment sg = sched.seg(s);
     const int L = seg_len(c, sched, a, s);
     const int nt = segment_tiles(sg, L);
     const int32_t* bt = a.block_table + (size_t)sg.req * a.bt_stride;
@@ -343,14 +370,14 @@ __device__ void producer(const Ctx& c, const Schedule<CAP>& sched, const DecodeA
 // written as zeros so 0-probability keys cannot inject NaN/Inf into P.V.
 // k_scale is not applied here: it is folded into the score scale and the
 // output scale.
-template <int CAP>
-__device__ void converter(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, int worker) {
+template <class S>
+__device__ void converter(const Ctx& c, const S& sched, const DecodeArgs& a, int worker) {
   const int w = (threadIdx.x >> 5) - 2;  // 0 or 1
   const int lane = threadIdx.x & 31;
   int j = 0;
   bool ok = true;
-  for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
-    const Segment sg = sched.seg[s];
+  for (int s = sched.begin(worker); ok && s < sched.end(worker); ++s) {
+    const Segment sg = sched.seg(s);
     const int L = seg_len(c, sched, a, s);
     const int nt = segment_tiles(sg, L);
     for (int jj = 0; jj < nt; ++jj, ++j) {
@@ -412,22 +439,22 @@ __device__ void converter(const Ctx& c, const Schedule<CAP>& sched, const Decode
 
 // ------------------------------------------------------------------ MMA issuer
 
-template <int CAP, bool F8>
-__device__ void mma_issuer(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, uint32_t tmem, int worker) {
+template <class S, bool F8>
+__device__ void mma_issuer(const Ctx& c, const S& sched, const DecodeArgs& a, uint32_t tmem, int worker) {
   constexpr int NS = op_stages<F8>();
   constexpr uint32_t kIdescS = idesc_s<F8>(), kIdescPV = idesc_pv<F8>();
   // Two cursors walk this worker's tile sequence: S products run ahead as
   // soon as a cache tile has landed and the S buffer they write was read by
   // the softmax warps; P.V products follow as P tiles appear.  Whichever is
   // ready is issued, so S of tile j+2 never waits for P.V of tile j.
-  const int seg_end = sched.worker_seg[worker + 1];
+  const int seg_end = sched.end(worker);
   auto first_live = [&](int s) {
-    while (s < seg_end && segment_tiles(sched.seg[s], seg_len(c, sched, a, s)) == 0) ++s;
+    while (s < seg_end && segment_tiles(sched.seg(s), seg_len(c, sched, a, s)) == 0) ++s;
     return s;
   };
-  int s_seg = first_live(sched.worker_seg[worker]), s_jj = 0, s_j = 0, q_used = 0;
+  int s_seg = first_live(sched.begin(worker)), s_jj = 0, s_j = 0, q_used = 0;
   int p_seg = s_seg, p_jj = 0, p_j = 0;
-  int s_nt = s_seg < seg_end ? segment_tiles(sched.seg[s_seg], seg_len(c, sched, a, s_seg)) : 0;
+  int s_nt = s_seg < seg_end ? segment_tiles(sched.seg(s_seg), seg_len(c, sched, a, s_seg)) : 0;
   int p_nt = s_nt;
   long long t_last = clock64();
   while (p_seg < seg_end) {
@@ -459,7 +486,7 @@ __device__ void mma_issuer(const Ctx& c, const Schedule<CAP>& sched, const Decod
         if (++s_jj == s_nt) {
           s_jj = 0;
           s_seg = first_live(s_seg + 1);
-          s_nt = s_seg < seg_end ? segment_tiles(sched.seg[s_seg], seg_len(c, sched, a, s_seg)) : 0;
+          s_nt = s_seg < seg_end ? segment_tiles(sched.seg(s_seg), seg_len(c, sched, a, s_seg)) : 0;
         }
         progressed = true;
       }
@@ -483,7 +510,7 @@ __device__ void mma_issuer(const Ctx& c, const Schedule<CAP>& sched, const Decod
       if (++p_jj == p_nt) {
         p_jj = 0;
         p_seg = first_live(p_seg + 1);
-        p_nt = p_seg < seg_end ? segment_tiles(sched.seg[p_seg], seg_len(c, sched, a, p_seg)) : 0;
+        p_nt = p_seg < seg_end ? segment_tiles(sched.seg(p_seg), seg_len(c, sched, a, p_seg)) : 0;
       }
       progressed = true;
     }
@@ -527,8 +554,8 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int CAP, bool F8>
-__device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, uint32_t tmem, int worker,
+template <class S, bool F8>
+__device__ void exchanger(const Ctx& c, const S& sched, const DecodeArgs& a, uint32_t tmem, int worker,
                           int rank) {
   const int quad = (threadIdx.x >> 5) & 3;
   const int lane = threadIdx.x & 31;
@@ -539,10 +566,14 @@ __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const Decode
   const uint32_t x_full_peer = mapa(c.bar(B_X_FULL), peer);  // slot k's barrier at + 8k
   const int M = a.rows;
   const bool valid_row = row < M;  // padding rows (M < 128) exchange nothing
+  // A warp whose rows are all padding sends nothing, so it must not wait on
+  // the "read" notes either: those phases are paced by the live rows alone
+  // and could run two phases ahead of it (a parity wait would then hang).
+  const bool warp_live = 32 * quad < M;
   int j = 0;
   bool ok = true;
-  for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
-    const Segment sg = sched.seg[s];
+  for (int s = sched.begin(worker); ok && s < sched.end(worker); ++s) {
+    const Segment sg = sched.seg(s);
     const int nt = segment_tiles(sg, seg_len(c, sched, a, s));
     if (nt == 0) continue;
     // ---- this segment's query: latent half -> TMEM columns [384, 512), rope
@@ -632,7 +663,10 @@ __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const Decode
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int g = 2 * j + h, k = g % kSlots, ug = g / kSlots;
-        if (ug > 0 && !wait_bar_warp<true>(c, c.bar(B_X_EMPTY + k), (ug - 1) & 1, 0x402)) { ok = false; break; }
+        if (warp_live && ug > 0 && !wait_bar_warp<true>(c, c.bar(B_X_EMPTY + k), (ug - 1) & 1, 0x402)) {
+          ok = false;
+          break;
+        }
         const uint32_t dst = xchg_peer + k * kSlotBytes;
         const uint32_t mb = x_full_peer + 8 * k;
         const uint32_t* sv = sv64 + 32 * h;
@@ -650,12 +684,12 @@ __device__ void exchanger(const Ctx& c, const Schedule<CAP>& sched, const Decode
   // drain: the peer's notes for the last half tiles are the only remote
   // writes nothing else waits for; they must land before this CTA may exit
   // (half tile g sits in slot g % kSlots, phase g / kSlots)
-  for (int g = 2 * j - 1; ok && g >= 0 && g >= 2 * j - kSlots; --g)
+  for (int g = 2 * j - 1; warp_live && ok && g >= 0 && g >= 2 * j - kSlots; --g)
     if (!wait_bar_warp<true>(c, c.bar(B_X_EMPTY + g % kSlots), (g / kSlots) & 1, 0x403)) break;
 }
 
-template <int CAP, bool F8>
-__device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const DecodeArgs& a, uint32_t tmem,
+template <class S, bool F8>
+__device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs& a, uint32_t tmem,
                                  int worker, int rank) {
   // Two warps per TMEM lane quadrant: warp (4 + q) and (8 + q) own query rows
   // 32q..32q+31 (= TMEM lanes); `half` selects which 32 of a tile's 64 keys
@@ -668,6 +702,11 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
   const uint32_t peer = rank ^ 1;
   const int M = a.rows;
   const bool valid_row = row < M;
+  // A warp whose rows are all padding reads nothing from the exchange and
+  // sends no "read" note: it must not wait on the receive barriers, whose
+  // phases are paced by the live rows' notes alone and could run two phases
+  // ahead of it (its parity wait would then hang).  Its rows see no key.
+  const bool warp_live = 32 * quad < M;
   const int qi = valid_row ? row / a.num_heads : 0;  // query position of this row
   // Exchange ring slots hold [16-byte chunk][row] so a warp's stores are
   // contiguous; half tile g = 2j + half of this thread sits in slot g % 3.
@@ -681,8 +720,8 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
   int j = 0, nseg = 0;
   bool ok = true;
 
-  for (int s = sched.worker_seg[worker]; ok && s < sched.worker_seg[worker + 1]; ++s) {
-    const Segment sg = sched.seg[s];
+  for (int s = sched.begin(worker); ok && s < sched.end(worker); ++s) {
+    const Segment sg = sched.seg(s);
     const int L = seg_len(c, sched, a, s);
     const int nt = segment_tiles(sg, L);
     // visible keys of this row; rows past the request's query rows (ragged
@@ -712,10 +751,13 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
         // the next phase right away is safe: the peer cannot send into this
         // slot again before all "read" notes of this phase reached it.
         const int g = 2 * j + half, slot = g % kSlots, ug = g / kSlots;
-        if (!wait_bar_warp<true>(c, c.bar(B_X_FULL + slot), ug & 1, 0x303)) { ok = false; break; }
-        if (threadIdx.x == rearm_thread) mbar_arrive_expect_tx(c.bar(B_X_FULL + slot), 128 * M);
+        if (warp_live && !wait_bar_warp<true>(c, c.bar(B_X_FULL + slot), ug & 1, 0x303)) { ok = false; break; }
+        if (threadIdx.x == rearm_thread) mbar_arrive_expect_tx(c.bar(B_X_FULL + slot), 128 * M);  // row 0: live
         float x[32];
-        {
+        if (!warp_live) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(cur[k]);  // masked below: no visible key
+        } else {
           const uint32_t srcx = xchg_local + slot * kSlotBytes;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
@@ -803,6 +845,7 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
                          make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]));
         }
         fence_proxy_async_smem();
+        tc_fence_before();  // orders a rescale's TMEM stores to O before the P.V that follows
         mbar_arrive(c.bar(B_P_FULL));
       }
       if (!ok) break;
@@ -883,10 +926,12 @@ __device__ void softmax_epilogue(const Ctx& c, const Schedule<CAP>& sched, const
 
 // ------------------------------------------------------------------ kernel
 
-template <int CAP, bool F8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_kernel(const __grid_constant__ Schedule<CAP> sched, const __grid_constant__ DecodeArgs a,
-                  const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope) {
+// The whole kernel; `sched` is a kernel parameter (host plan) or lives in the
+// workspace (device plan, kDevSched: written by the planner grid that runs
+// just before, so it is read only after griddepcontrol.wait).
+template <class S, bool F8, bool kDevSched>
+__device__ __forceinline__ void decode_body(const S& sched, const DecodeArgs& a,
+                                            const CUtensorMap& tm_lat, const CUtensorMap& tm_rope) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -899,13 +944,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int worker = blockIdx.x >> 1;
   c.seg_len = reinterpret_cast<const int*>(c.smem + OFF_SEGLEN);
   c.seg_q = reinterpret_cast<const int2*>(c.smem + OFF_SEGQ);
-  c.seg0 = worker < sched.num_workers ? sched.worker_seg[worker] : 0;
-  if (warp == 2 && worker < sched.num_workers) {
+  // device plan: the schedule is complete and visible once this returns
+  // (only the launch itself overlapped the planner grid)
+  if (kDevSched) asm volatile("griddepcontrol.wait;" ::: "memory");
+  c.seg0 = worker < sched.num_workers() ? sched.begin(worker) : 0;
+  if (warp == 2 && worker < sched.num_workers()) {
     // key counts and query rows of this worker's segments, read once for
     // every role
-    const int n = min(sched.worker_seg[worker + 1] - c.seg0, kSegLenCache);
+    const int n = min(sched.end(worker) - c.seg0, kSegLenCache);
     for (int i = threadIdx.x & 31; i < n; i += 32) {
-      const int req = sched.seg[c.seg0 + i].req;
+      const int req = sched.seg(c.seg0 + i).req;
       reinterpret_cast<int*>(c.smem + OFF_SEGLEN)[i] = request_len(a, req);
       reinterpret_cast<int2*>(c.smem + OFF_SEGQ)[i] = request_q_checked(a, req);
     }
@@ -950,18 +998,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(c.smem + OFF_TMEM_SLOT);
 
-  if (worker < sched.num_workers) {
+  if (worker < sched.num_workers()) {
     if (warp == 0) {
-      producer<CAP, F8>(c, sched, a, &tm_lat, &tm_rope, worker, rank);
+      producer<S, F8>(c, sched, a, &tm_lat, &tm_rope, worker, rank);
     } else if (warp == 1) {
-      if ((threadIdx.x & 31) == 0) mma_issuer<CAP, F8>(c, sched, a, tmem, worker);
+      if ((threadIdx.x & 31) == 0) mma_issuer<S, F8>(c, sched, a, tmem, worker);
       __syncwarp();
     } else if (warp >= 12) {
-      exchanger<CAP, F8>(c, sched, a, tmem, worker, rank);
+      exchanger<S, F8>(c, sched, a, tmem, worker, rank);
     } else if (warp >= 4) {
-      softmax_epilogue<CAP, F8>(c, sched, a, tmem, worker, rank);
+      softmax_epilogue<S, F8>(c, sched, a, tmem, worker, rank);
     } else if (F8) {
-      converter<CAP>(c, sched, a, worker);
+      converter<S>(c, sched, a, worker);
     }
   }
 
@@ -974,6 +1022,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
   cluster_sync();  // no peer may still write into this CTA's shared memory
+}
+
+template <int CAP, bool F8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ Schedule<CAP> sched, const __grid_constant__ DecodeArgs a,
+                  const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope) {
+  decode_body<ParamSched<CAP>, F8, false>(ParamSched<CAP>{sched}, a, tm_lat, tm_rope);
+}
+
+// Device-planned variant: the schedule is in the workspace.
+template <bool F8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_kernel_dev(const Schedule<kSegCapLarge>* sched, const __grid_constant__ DecodeArgs a,
+                      const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope) {
+  decode_body<GlobalSched, F8, true>(GlobalSched{sched}, a, tm_lat, tm_rope);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1028,8 +1091,36 @@ static cudaError_t launch_cap(const mla_plan& p, const DecodeArgs& a, const CUte
   return cudaGetLastError();
 }
 
+// Device plan: the schedule sits at the head of the workspace, written by the
+// planner grid launched just before on the same stream; this launch is its
+// programmatic dependent (see decode_body).
 template <bool F8>
-static cudaError_t launch_dtype(const mla_plan& p, const DecodeArgs& a, cudaStream_t stream) {
+static cudaError_t launch_dev(const mla_plan& p, const DecodeArgs& a, const CUtensorMap& lat,
+                              const CUtensorMap& rope, const void* workspace, cudaStream_t stream) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(decode_kernel_dev<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const auto* sched = reinterpret_cast<const Schedule<kSegCapLarge>*>(static_cast<const char*>(workspace) +
+                                                                       kDevSchedOffset);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * p.num_workers);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel_dev<F8>, sched, a, lat, rope);
+}
+
+template <bool F8>
+static cudaError_t launch_dtype(const mla_plan& p, const DecodeArgs& a, const void* workspace,
+                                cudaStream_t stream) {
   CUtensorMap lat, rope;
   const int64_t rows = a.num_pages * a.page_size;
   // bf16: four 64-column 128B-swizzled latent boxes + one 32-column 64B-swizzled
@@ -1040,6 +1131,7 @@ static cudaError_t launch_dtype(const mla_plan& p, const DecodeArgs& a, cudaStre
                      : make_map(&lat, a.kv, rows, 64, a.page_size, CU_TENSOR_MAP_SWIZZLE_128B, false) &&
                            make_map(&rope, a.kv, rows, 32, a.page_size, CU_TENSOR_MAP_SWIZZLE_64B, false);
   if (!ok) return cudaErrorNotSupported;
+  if (p.device) return launch_dev<F8>(p, a, lat, rope, workspace, stream);
   if (p.segs.size() <= (size_t)kSegCapSmall) return launch_cap<kSegCapSmall, F8>(p, a, lat, rope, stream);
   return launch_cap<kSegCapLarge, F8>(p, a, lat, rope, stream);
 }
@@ -1047,9 +1139,10 @@ static cudaError_t launch_dtype(const mla_plan& p, const DecodeArgs& a, cudaStre
 }  // namespace sm103
 
 // Returns cudaErrorNotSupported when the tensor-map encoder is unavailable.
-cudaError_t launch_sm103(const mla_plan& p, const DecodeArgs& a, cudaStream_t stream) {
-  return a.kv_dtype == MLA_KV_E4M3 ? sm103::launch_dtype<true>(p, a, stream)
-                                   : sm103::launch_dtype<false>(p, a, stream);
+// `workspace` is read only for a device plan (its schedule area).
+cudaError_t launch_sm103(const mla_plan& p, const DecodeArgs& a, const void* workspace, cudaStream_t stream) {
+  return a.kv_dtype == MLA_KV_E4M3 ? sm103::launch_dtype<true>(p, a, workspace, stream)
+                                   : sm103::launch_dtype<false>(p, a, workspace, stream);
 }
 
 // Kernel-side error code recorded since the last reset (0 = none).
