@@ -430,9 +430,23 @@ def device_plan_measure(db, w, dev, stream, flush, K, st):
         ev[k][1].record(stream)
     torch.cuda.synchronize()
     s_avg = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    # the two launches apart: planner + main kernel, then the combine
+    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for k in range(K):
+        flush.zero_()
+        evk[k][0].record(stream)
+        B.mla_decode_main(plan, db.q_nope, db.q_pe, db.kv, db.kv_dtype, db.block_table, db.seq_lens, w.scale,
+                          w.k_scale, out, lse, ws, None, stream)
+        evk[k][1].record(stream)
+        B.mla_decode_combine(plan, out, lse, ws, None, stream)
+        evk[k][2].record(stream)
+    torch.cuda.synchronize()
+    main_us = statistics.mean(e[0].elapsed_time(e[1]) for e in evk) * 1e3
+    comb_us = statistics.mean(e[1].elapsed_time(e[2]) for e in evk) * 1e3
     host_out = R.decode(db, stream)[0]
     diff = float((out.float() - host_out.float()).abs().max())  # the two plans split differently
     return {"us_per_step": s_avg * 1e6, "tokens_per_s": st["tokens"] / s_avg,
+            "planner_plus_main_us": main_us, "combine_us": comb_us,
             "segments": int(len(plan.device_segments(ws))), "launches_per_step": 3,
             "max_abs_diff_vs_host_plan": diff,
             "note": "planner + main + combine per step, L2 flushed between steps"}
@@ -553,15 +567,42 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed steps before timing")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="run --warmup + 1 decode steps of --config and exit: a small, fixed launch sequence "
+                         "for ncu captures (no timing, no JSON line)")
+    ap.add_argument("--pool-pages", type=int, default=0,
+                    help="with --profile: cache pool size in pages (0 = the workload's); the decode reads the "
+                         "same pages either way, and a smaller pool keeps a capture's device memory small")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     # weak scaling: every rank decodes its own batch of the same shape
-    w = W.make_workload(args.config, seed=args.seed + rank)
+    extra = {"pool_pages": args.pool_pages} if (args.profile and args.pool_pages) else {}
+    w = W.make_workload(args.config, seed=args.seed + rank, **extra)
     if args.impl == "reference":
         reference_arm(args, w, rank)
         return
+    if args.profile:
+        profile_run(args, w)
+        return
     our_arm(args, w, rank, world)
+
+
+def profile_run(args, w):
+    """The launch sequence ncu captures: (warmup + 1) x [L2 flush, mla_decode]
+    on the configured workload (main kernel then combine per step)."""
+    import torch
+    from paged_mla_decode_08_gb300 import runner as R
+    from paged_mla_decode_08_gb300.build import build
+    build()
+    db = R.upload(w)
+    flush = torch.empty(2 * int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 128 << 20)),
+                        dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup + 1):
+        flush.zero_()
+        R.decode(db)
+    torch.cuda.synchronize()
+    print(f"profile run: {args.warmup + 1} decode steps of {w.name}", flush=True)
 
 
 if __name__ == "__main__":

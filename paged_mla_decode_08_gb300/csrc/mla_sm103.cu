@@ -89,7 +89,8 @@ constexpr int kNoteBytes = 128 * 4;
 constexpr int OFF_SEGLEN = OFF_SINK + kSlots * kNoteBytes;  // key counts of the worker's first segments
 constexpr int kSegLenCache = 64;
 constexpr int OFF_SEGQ = OFF_SEGLEN + kSegLenCache * 4;     // ... and their (first token, query count)
-constexpr int OFF_BAR = OFF_SEGQ + kSegLenCache * 8;
+constexpr int OFF_SEGS = OFF_SEGQ + kSegLenCache * 8;       // device plan: the segments themselves
+constexpr int OFF_BAR = OFF_SEGS + kSegLenCache * 16;
 enum Bar : int {
   B_KV_FULL = 0, B_KV_EMPTY = B_KV_FULL + kStages, B_S_FULL = B_KV_EMPTY + kStages, B_P_FULL = B_S_FULL + 2,
   B_PV_DONE, B_Q_READY, B_X_FULL, B_X_EMPTY = B_X_FULL + kSlots, B_TAIL = B_X_EMPTY + kSlots, B_FINAL,
@@ -138,6 +139,7 @@ struct Ctx {
 template <int CAP>
 struct ParamSched {
   const Schedule<CAP>& s;
+  __device__ __forceinline__ const void* raw() const { return &s; }
   __device__ __forceinline__ int num_workers() const { return s.num_workers; }
   __device__ __forceinline__ int begin(int w) const { return s.worker_seg[w]; }
   __device__ __forceinline__ int end(int w) const { return s.worker_seg[w + 1]; }
@@ -145,12 +147,32 @@ struct ParamSched {
 };
 struct GlobalSched {
   const Schedule<kSegCapLarge>* s;
+  __device__ __forceinline__ const void* raw() const { return s; }
   __device__ __forceinline__ int num_workers() const { return __ldcg(&s->num_workers); }
   __device__ __forceinline__ int begin(int w) const { return __ldcg(&s->worker_seg[w]); }
   __device__ __forceinline__ int end(int w) const { return __ldcg(&s->worker_seg[w + 1]); }
   // four 4-byte loads: the segment array is only 4-byte aligned (it follows
   // the 4-byte header fields), so no vector load may touch it
   __device__ __forceinline__ Segment seg(int i) const {
+    const Segment* p = &s->seg[i];
+    return Segment{__ldcg(&p->req), __ldcg(&p->tile_begin), __ldcg(&p->tile_end), __ldcg(&p->slot)};
+  }
+};
+
+// A device plan's schedule once the prologue has copied this worker's first
+// kSegLenCache segments into shared memory: the roles read those like the
+// host plan's kernel parameter (no L2 round trip at a segment switch);
+// segments past them are read at L2.  begin/end answer for this CTA's own
+// worker only.
+struct CachedSched {
+  const Schedule<kSegCapLarge>* s;
+  const Segment* cache;  // shared memory: segments first .. first + cached - 1
+  int first, last, cached, workers;
+  __device__ __forceinline__ int num_workers() const { return workers; }
+  __device__ __forceinline__ int begin(int) const { return first; }
+  __device__ __forceinline__ int end(int) const { return last; }
+  __device__ __forceinline__ Segment seg(int i) const {
+    if (i - first < cached) return cache[i - first];
     const Segment* p = &s->seg[i];
     return Segment{__ldcg(&p->req), __ldcg(&p->tile_begin), __ldcg(&p->tile_end), __ldcg(&p->slot)};
   }
@@ -926,6 +948,24 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
 
 // ------------------------------------------------------------------ kernel
 
+template <class R, bool F8>
+__device__ __forceinline__ void run_roles(const Ctx& c, const R& sched, const DecodeArgs& a, uint32_t tmem,
+                                          int worker, int rank, int warp, const CUtensorMap& tm_lat,
+                                          const CUtensorMap& tm_rope) {
+  if (warp == 0) {
+    producer<R, F8>(c, sched, a, &tm_lat, &tm_rope, worker, rank);
+  } else if (warp == 1) {
+    if ((threadIdx.x & 31) == 0) mma_issuer<R, F8>(c, sched, a, tmem, worker);
+    __syncwarp();
+  } else if (warp >= 12) {
+    exchanger<R, F8>(c, sched, a, tmem, worker, rank);
+  } else if (warp >= 4) {
+    softmax_epilogue<R, F8>(c, sched, a, tmem, worker, rank);
+  } else if (F8) {
+    converter<R>(c, sched, a, worker);
+  }
+}
+
 // The whole kernel; `sched` is a kernel parameter (host plan) or lives in the
 // workspace (device plan, kDevSched: written by the planner grid that runs
 // just before, so it is read only after griddepcontrol.wait).
@@ -944,20 +984,21 @@ __device__ __forceinline__ void decode_body(const S& sched, const DecodeArgs& a,
   const int worker = blockIdx.x >> 1;
   c.seg_len = reinterpret_cast<const int*>(c.smem + OFF_SEGLEN);
   c.seg_q = reinterpret_cast<const int2*>(c.smem + OFF_SEGQ);
-  // device plan: the schedule is complete and visible once this returns
-  // (only the launch itself overlapped the planner grid)
-  if (kDevSched) asm volatile("griddepcontrol.wait;" ::: "memory");
-  c.seg0 = worker < sched.num_workers() ? sched.begin(worker) : 0;
-  if (warp == 2 && worker < sched.num_workers()) {
-    // key counts and query rows of this worker's segments, read once for
-    // every role
-    const int n = min(sched.end(worker) - c.seg0, kSegLenCache);
-    for (int i = threadIdx.x & 31; i < n; i += 32) {
-      const int req = sched.seg(c.seg0 + i).req;
-      reinterpret_cast<int*>(c.smem + OFF_SEGLEN)[i] = request_len(a, req);
-      reinterpret_cast<int2*>(c.smem + OFF_SEGQ)[i] = request_q_checked(a, req);
+  // key counts and query rows of this worker's segments (and, for a device
+  // plan, the segments themselves), read once for every role
+  auto read_schedule = [&]() {
+    c.seg0 = worker < sched.num_workers() ? sched.begin(worker) : 0;
+    if (warp == 2 && worker < sched.num_workers()) {
+      const int n = min(sched.end(worker) - c.seg0, kSegLenCache);
+      for (int i = threadIdx.x & 31; i < n; i += 32) {
+        const Segment sg = sched.seg(c.seg0 + i);
+        reinterpret_cast<int*>(c.smem + OFF_SEGLEN)[i] = request_len(a, sg.req);
+        reinterpret_cast<int2*>(c.smem + OFF_SEGQ)[i] = request_q_checked(a, sg.req);
+        if (kDevSched) reinterpret_cast<Segment*>(c.smem + OFF_SEGS)[i] = sg;
+      }
     }
-  }
+  };
+  if (!kDevSched) read_schedule();
 
   if (threadIdx.x == 0) {
     *c.abort_flag = 0;
@@ -992,6 +1033,12 @@ __device__ __forceinline__ void decode_body(const S& sched, const DecodeArgs& a,
     tmem_alloc(c.sbase + OFF_TMEM_SLOT, kTmemCols);
     tmem_relinquish();
   }
+  // device plan: all of the above overlapped the planner grid; the schedule
+  // is complete and visible once this returns
+  if (kDevSched) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    read_schedule();
+  }
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // peer barriers initialised before any remote arrive
@@ -999,17 +1046,14 @@ __device__ __forceinline__ void decode_body(const S& sched, const DecodeArgs& a,
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(c.smem + OFF_TMEM_SLOT);
 
   if (worker < sched.num_workers()) {
-    if (warp == 0) {
-      producer<S, F8>(c, sched, a, &tm_lat, &tm_rope, worker, rank);
-    } else if (warp == 1) {
-      if ((threadIdx.x & 31) == 0) mma_issuer<S, F8>(c, sched, a, tmem, worker);
-      __syncwarp();
-    } else if (warp >= 12) {
-      exchanger<S, F8>(c, sched, a, tmem, worker, rank);
-    } else if (warp >= 4) {
-      softmax_epilogue<S, F8>(c, sched, a, tmem, worker, rank);
-    } else if (F8) {
-      converter<S>(c, sched, a, worker);
+    if (kDevSched) {
+      const int last = sched.end(worker);
+      const CachedSched cs{static_cast<const Schedule<kSegCapLarge>*>(sched.raw()),
+                           reinterpret_cast<const Segment*>(c.smem + OFF_SEGS), c.seg0, last,
+                           min(last - c.seg0, kSegLenCache), sched.num_workers()};
+      run_roles<CachedSched, F8>(c, cs, a, tmem, worker, rank, warp, tm_lat, tm_rope);
+    } else {
+      run_roles<S, F8>(c, sched, a, tmem, worker, rank, warp, tm_lat, tm_rope);
     }
   }
 
