@@ -139,10 +139,14 @@ def mla_decode(
     scale: float,
     k_scale: float = 1.0,
     requests=None,
+    q_dtype: str = "bf16",
 ):
     """Reference decode over stored inputs.
 
-    q_nope_bits uint16 [T,H,512], q_pe_bits uint16 [T,H,64] (bf16 bits);
+    q_nope_bits [T,H,512], q_pe_bits [T,H,64]: uint16 bf16 bits, or with
+    q_dtype="e4m3" uint8 e4m3fn codes (the merged FP8 query of the pages'
+    FP8 path, split at column 512; decoded exactly, no query scale: sglang
+    trtllm_mla_backend.py, _compute_decode_bmm1_scale takes q_scale = 1);
     kv_bits [P,page,576] (uint16 bf16 bits or uint8 e4m3fn codes).
     Returns float64 (out [T,H,512], lse [T,H]); with ``requests`` given, only
     those requests' rows are filled (the rest stay NaN).
@@ -158,7 +162,7 @@ def mla_decode(
             tok = b * q_len + i
             v = max(n - q_len + 1 + i, 0)
             out[tok], lse[tok] = attend(
-                decode_bf16(q_nope_bits[tok]), decode_bf16(q_pe_bits[tok]), rows[:v], scale
+                decode(q_nope_bits[tok], q_dtype), decode(q_pe_bits[tok], q_dtype), rows[:v], scale
             )
     return out, lse
 

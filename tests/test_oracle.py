@@ -333,3 +333,20 @@ def test_golden_tiny():
     assert np.allclose(lse.reshape(-1), stored["lse"], rtol=0, atol=1e-12)
     assert np.allclose(out.reshape(-1)[:: 97], stored["out_every_97th"], rtol=0, atol=1e-12)
     assert np.allclose(out.sum(axis=-1).reshape(-1), stored["out_row_sums"], rtol=0, atol=1e-10)
+
+
+def test_e4m3_query_is_its_exact_value():
+    """An e4m3 query decodes to the same numbers as its exact bf16 form
+    (every e4m3 value is a bf16 value): the two decodes agree bit for bit."""
+    from paged_mla_decode_08_gb300 import workloads as W
+    rng = np.random.default_rng(31)
+    w = W.make_workload("tiny", seed=31, kv_dtype="e4m3", k_scale=0.5, seq_lens=[70, 1, 0], num_heads=4)
+    qn8 = W.f32_to_e4m3fn_bits(rng.standard_normal(w.q_nope_bits.shape).astype(np.float32))
+    qp8 = W.f32_to_e4m3fn_bits(rng.standard_normal(w.q_pe_bits.shape).astype(np.float32))
+    qn16 = W.f32_to_bf16_bits(O.decode_e4m3fn(qn8).astype(np.float32))
+    qp16 = W.f32_to_bf16_bits(O.decode_e4m3fn(qp8).astype(np.float32))
+    assert np.array_equal(O.decode_bf16(qn16), O.decode_e4m3fn(qn8))  # exact
+    a = O.mla_decode(qn8, qp8, w.kv_bits, "e4m3", w.block_table, w.seq_lens, 1, w.page_size, w.scale, 0.5,
+                     q_dtype="e4m3")
+    b = O.mla_decode(qn16, qp16, w.kv_bits, "e4m3", w.block_table, w.seq_lens, 1, w.page_size, w.scale, 0.5)
+    assert np.array_equal(a[0], b[0], equal_nan=True) and np.array_equal(a[1], b[1])
