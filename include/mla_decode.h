@@ -198,6 +198,26 @@ int mla_decode_ragged(const mla_plan* plan, const void* q_nope, const void* q_pe
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * mla_decode_fp8q -- the decode of the pages' FP8 path: an e4m3 cache and
+ * the merged e4m3 query that mla_rope_quantize_cache_write (MLA_Q_E4M3)
+ * produces (sglang trtllm_mla_backend.py, forward_decode: the output of
+ * mla_quantize_and_rope_for_fp8 goes to the decode kernel as
+ * q.view(-1, H, 576); _compute_decode_bmm1_scale uses q_scale = 1).
+ *
+ *   q             device e4m3 [num_tokens, num_heads, 576] = [q_nope | q_pe],
+ *                 16-byte aligned; no query scale.
+ *   cu_seqlens_q  NULL for a uniform batch (num_tokens = batch * q_len), or
+ *                 the ragged offsets of mla_decode_ragged.
+ * Everything else as mla_decode with kv_dtype = MLA_KV_E4M3.  The query's
+ * values are exact in fp16, so the result equals mla_decode's over the
+ * same values given as bf16.
+ */
+int mla_decode_fp8q(const mla_plan* plan, const void* q, int num_tokens, int num_heads, const void* kv_pages,
+                    int64_t num_pages, int page_size, const int32_t* block_table, int bt_stride,
+                    const int32_t* seq_lens, const int32_t* cu_seqlens_q, float scale, float k_scale, void* out,
+                    float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mla_decode_noalloc -- the decode for callers that cannot allocate device
  * memory.  (No counterpart on the serving pages: their backends always own a
  * workspace buffer; this entry point is this library's own addition.)

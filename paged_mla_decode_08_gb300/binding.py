@@ -47,6 +47,8 @@ SIGNATURES = {
     "mla_rope_quantize_cache_write": (_c_int, [_vp, _vp, _c_int, _c_int, _vp, _c_int, _vp, _vp, _vp, _vp,
                                                ctypes.c_int64, _c_int, _vp, _c_int, ctypes.c_int64, _c_int, _vp,
                                                _vp]),
+    "mla_decode_fp8q": (_c_int, [_vp, _vp, _c_int, _c_int, _vp, ctypes.c_int64, _c_int, _vp, _c_int, _vp, _vp,
+                                 ctypes.c_float, ctypes.c_float, _vp, _vp, _vp, _c_size, _vp]),
     "mla_block_table_from_tokens": (_c_int, [_vp, ctypes.c_int64, ctypes.c_int64, _vp, _vp, _c_int, _c_int,
                                              _vp, _c_int, _vp]),
     "mla_block_table_from_pages": (_c_int, [_vp, ctypes.c_int64, ctypes.c_int64, _vp, _c_int, _vp, _c_int,
@@ -223,6 +225,18 @@ def mla_decode_ragged(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_t
     args = _decode_args(plan, q_nope, q_pe, kv_pages, kv_dtype, block_table, seq_lens, scale, k_scale, out, lse,
                         workspace, workspace_bytes, stream)
     _check(load().mla_decode_ragged(*args[:12], _ptr(cu_seqlens_q), *args[12:]))
+
+
+def mla_decode_fp8q(plan: Plan, q, kv_pages, block_table, seq_lens, scale: float, k_scale: float, out, lse,
+                    workspace=None, workspace_bytes=None, cu_seqlens_q=None, stream=None):
+    """Decode with the merged e4m3 query ``q`` [T, H, 576] over an e4m3 cache."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().mla_decode_fp8q(plan.handle, _ptr(q), int(q.shape[0]), int(q.shape[1]), _ptr(kv_pages),
+                                  int(kv_pages.shape[0]), int(kv_pages.shape[1]), _ptr(block_table),
+                                  int(block_table.shape[1]), _ptr(seq_lens), _ptr(cu_seqlens_q), float(scale),
+                                  float(k_scale), _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                                  _stream(stream)))
 
 
 def mla_decode_main(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_table, seq_lens, scale: float,

@@ -133,6 +133,7 @@ int prepare(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_
   a.out_scale = kf;
   a.cu_q = cu_seqlens_q;
   a.num_tokens = num_tokens;
+  a.q_e4m3 = 0;
   return MLA_OK;
 }
 
@@ -334,6 +335,29 @@ int mla_plan_read_device_schedule(const mla_plan* plan, const void* workspace, i
   delete h;
   ok();
   return copied;
+}
+
+int mla_decode_fp8q(const mla_plan* plan, const void* q, int num_tokens, int num_heads, const void* kv_pages,
+                    int64_t num_pages, int page_size, const int32_t* block_table, int bt_stride,
+                    const int32_t* seq_lens, const int32_t* cu_seqlens_q, float scale, float k_scale, void* out,
+                    float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q) return fail(MLA_ERR_ARG, "q is NULL");
+  Prepared pr;
+  // q stands in for both query pointers in the shared checks; the kernel
+  // reads it as merged rows
+  int rc = prepare(plan, q, q, num_tokens, num_heads, kv_pages, MLA_KV_E4M3, num_pages, page_size, block_table,
+                   bt_stride, seq_lens, cu_seqlens_q, scale, k_scale, out, lse, workspace, workspace_bytes, &pr);
+  if (rc != MLA_OK) return rc;
+  if (!aligned(q, 16)) return fail(MLA_ERR_ARG, "q must be 16-byte aligned");
+  pr.args.q_e4m3 = 1;
+  pr.args.q_pe = nullptr;
+  rc = check_device(nullptr);
+  if (rc != MLA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = launch_main(plan, pr, s);
+  if (rc != MLA_OK) return rc;
+  rc = launch_combine(plan, pr, s);
+  return rc == MLA_OK ? ok() : rc;
 }
 
 size_t mla_plan_workspace_bytes(const mla_plan* plan) { return plan ? plan->ws_bytes : 0; }

@@ -91,6 +91,7 @@ struct DecodeArgs {
   const int32_t* cu_q;     // ragged batches: int32 [batch + 1] first query token of each
                            // request (q_len is then the planned maximum); nullptr: uniform
   int32_t num_tokens;      // rows of q_nope / q_pe / out / lse
+  int32_t q_e4m3;          // q_nope is the merged e4m3 query [T, H, 576] (q_pe unused)
 };
 
 #ifdef __CUDACC__

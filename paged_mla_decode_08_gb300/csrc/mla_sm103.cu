@@ -249,7 +249,7 @@ __device__ __forceinline__ int segment_tiles(const Segment& sg, int L) {
 
 // ------------------------------------------------------------------ producer
 
-template <class S, bool F8>
+template <class S, bool F8, bool Q8>
 __device__ void producer(const Ctx& c, const S& sched, const DecodeArgs& a, const CUtensorMap* tm_lat,
                          const CUtensorMap* tm_rope, int worker, int rank) {
   const int lane = threadIdx.x & 31;
@@ -288,7 +288,9 @@ __device__ void producer(const Ctx& c, const S& sched, const DecodeArgs& a, cons
       const int2 q = seg_q(c, sched, a, s);
       const size_t r0 = (size_t)q.x * a.num_heads;
       const uint32_t nr = (uint32_t)(q.y * a.num_heads);
-      if (nr > 0) {
+      if (nr > 0 && Q8) {
+        prefetch_l2_bulk(static_cast<const uint8_t*>(a.q_nope) + r0 * kKvDim, nr * kKvDim);  // merged e4m3 rows
+      } else if (nr > 0) {
         prefetch_l2_bulk(reinterpret_cast<const __nv_bfloat16*>(a.q_nope) + r0 * kLatent, nr * kLatent * 2);
         prefetch_l2_bulk(reinterpret_cast<const __nv_bfloat16*>(a.q_pe) + r0 * kRope, nr * kRope * 2);
       }
@@ -576,7 +578,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <class S, bool F8>
+template <class S, bool F8, bool Q8>
 __device__ void exchanger(const Ctx& c, const S& sched, const DecodeArgs& a, uint32_t tmem, int worker,
                           int rank) {
   const int quad = (threadIdx.x >> 5) & 3;
@@ -614,20 +616,37 @@ __device__ void exchanger(const Ctx& c, const S& sched, const DecodeArgs& a, uin
       const size_t row0 = (size_t)q.x * a.num_heads + 32 * quad;
       const uint4* qn = reinterpret_cast<const uint4*>(a.q_nope) + row0 * (kLatent / 8) + 32 * rank + qc;
       const uint4* qp = reinterpret_cast<const uint4*>(a.q_pe) + row0 * (kRope / 8) + 4 * rank + qc;
+      // e4m3 query (Q8): merged [row][576] bytes; this lane's 8 columns are 8 bytes
+      const uint2* q8 = reinterpret_cast<const uint2*>(a.q_nope) + row0 * (kKvDim / 8) + 32 * rank + qc;
       const uint32_t stage = c.sbase + OFF_QROPE + quad * 2048;  // this warp's rows of the rope area
       auto lrow_ok = [&](int rl) { return 32 * quad + rl < rows_b; };
+      // 8 e4m3 values -> 8 fp16 (exact)
+      auto widen = [&](uint2 v) {
+        return make_uint4(cvt_e4m3x2_f16x2(v.x), cvt_e4m3x2_f16x2(v.x >> 16), cvt_e4m3x2_f16x2(v.y),
+                          cvt_e4m3x2_f16x2(v.y >> 16));
+      };
+      // 8 latent columns of row rl, chunk cidx (8-column units within this CTA's half)
+      auto load_lat = [&](int rl, int cidx) {
+        if (!lrow_ok(rl)) return make_uint4(0, 0, 0, 0);
+        if (Q8) return widen(__ldg(q8 + (size_t)rl * (kKvDim / 8) + cidx));
+        return __ldg(qn + (size_t)rl * (kLatent / 8) + cidx);
+      };
+      auto load_rope = [&](int rl) {
+        if (!lrow_ok(rl)) return make_uint4(0, 0, 0, 0);
+        if (Q8) return widen(__ldg(q8 + (size_t)rl * (kKvDim / 8) + (kLatent / 8) - 28 * rank));
+        return __ldg(qp + (size_t)rl * (kRope / 8));
+      };
+      // bf16 -> fp16 for the e4m3 cache's fp16 MMAs (an e4m3 query is fp16 already)
       auto cvt4 = [&](uint4 v) {
-        return F8 ? make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w))
-                  : v;
+        return (F8 && !Q8)
+                   ? make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w))
+                   : v;
       };
       uint4 rpe[4], lat[4][4];
 #pragma unroll
       for (int rd = 0; rd < 4; ++rd)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int rl = 8 * k + ql;
-          lat[rd][k] = lrow_ok(rl) ? __ldg(qn + (size_t)rl * (kLatent / 8) + 4 * rd) : make_uint4(0, 0, 0, 0);
-        }
+        for (int k = 0; k < 4; ++k) lat[rd][k] = load_lat(8 * k + ql, 4 * rd);
       // piece p (0..7) = latent columns [32p, 32p+32) of this CTA's half =
       // TMEM columns TM_Q + 16p; piece p + 4 is requested as piece p retires
 #pragma unroll
@@ -641,16 +660,10 @@ __device__ void exchanger(const Ctx& c, const S& sched, const DecodeArgs& a, uin
         __syncwarp();
         if (pc < 4) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int rl = 8 * k + ql;
-            lat[rd][k] = lrow_ok(rl) ? __ldg(qn + (size_t)rl * (kLatent / 8) + 4 * (rd + 4)) : make_uint4(0, 0, 0, 0);
-          }
+          for (int k = 0; k < 4; ++k) lat[rd][k] = load_lat(8 * k + ql, 4 * (rd + 4));
         } else if (pc == 4) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int rl = 8 * k + ql;
-            rpe[k] = lrow_ok(rl) ? __ldg(qp + (size_t)rl * (kRope / 8)) : make_uint4(0, 0, 0, 0);
-          }
+          for (int k = 0; k < 4; ++k) rpe[k] = load_rope(8 * k + ql);
         }
         uint32_t r[16];
 #pragma unroll
@@ -948,17 +961,17 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
 
 // ------------------------------------------------------------------ kernel
 
-template <class R, bool F8>
+template <class R, bool F8, bool Q8>
 __device__ __forceinline__ void run_roles(const Ctx& c, const R& sched, const DecodeArgs& a, uint32_t tmem,
                                           int worker, int rank, int warp, const CUtensorMap& tm_lat,
                                           const CUtensorMap& tm_rope) {
   if (warp == 0) {
-    producer<R, F8>(c, sched, a, &tm_lat, &tm_rope, worker, rank);
+    producer<R, F8, Q8>(c, sched, a, &tm_lat, &tm_rope, worker, rank);
   } else if (warp == 1) {
     if ((threadIdx.x & 31) == 0) mma_issuer<R, F8>(c, sched, a, tmem, worker);
     __syncwarp();
   } else if (warp >= 12) {
-    exchanger<R, F8>(c, sched, a, tmem, worker, rank);
+    exchanger<R, F8, Q8>(c, sched, a, tmem, worker, rank);
   } else if (warp >= 4) {
     softmax_epilogue<R, F8>(c, sched, a, tmem, worker, rank);
   } else if (F8) {
@@ -969,7 +982,7 @@ __device__ __forceinline__ void run_roles(const Ctx& c, const R& sched, const De
 // The whole kernel; `sched` is a kernel parameter (host plan) or lives in the
 // workspace (device plan, kDevSched: written by the planner grid that runs
 // just before, so it is read only after griddepcontrol.wait).
-template <class S, bool F8, bool kDevSched>
+template <class S, bool F8, bool kDevSched, bool Q8>
 __device__ __forceinline__ void decode_body(const S& sched, const DecodeArgs& a,
                                             const CUtensorMap& tm_lat, const CUtensorMap& tm_rope) {
   extern __shared__ uint8_t smem_raw[];
@@ -1051,9 +1064,9 @@ __device__ __forceinline__ void decode_body(const S& sched, const DecodeArgs& a,
       const CachedSched cs{static_cast<const Schedule<kSegCapLarge>*>(sched.raw()),
                            reinterpret_cast<const Segment*>(c.smem + OFF_SEGS), c.seg0, last,
                            min(last - c.seg0, kSegLenCache), sched.num_workers()};
-      run_roles<CachedSched, F8>(c, cs, a, tmem, worker, rank, warp, tm_lat, tm_rope);
+      run_roles<CachedSched, F8, Q8>(c, cs, a, tmem, worker, rank, warp, tm_lat, tm_rope);
     } else {
-      run_roles<S, F8>(c, sched, a, tmem, worker, rank, warp, tm_lat, tm_rope);
+      run_roles<S, F8, Q8>(c, sched, a, tmem, worker, rank, warp, tm_lat, tm_rope);
     }
   }
 
@@ -1068,19 +1081,19 @@ __device__ __forceinline__ void decode_body(const S& sched, const DecodeArgs& a,
   cluster_sync();  // no peer may still write into this CTA's shared memory
 }
 
-template <int CAP, bool F8>
+template <int CAP, bool F8, bool Q8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ Schedule<CAP> sched, const __grid_constant__ DecodeArgs a,
                   const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope) {
-  decode_body<ParamSched<CAP>, F8, false>(ParamSched<CAP>{sched}, a, tm_lat, tm_rope);
+  decode_body<ParamSched<CAP>, F8, false, Q8>(ParamSched<CAP>{sched}, a, tm_lat, tm_rope);
 }
 
 // Device-planned variant: the schedule is in the workspace.
-template <bool F8>
+template <bool F8, bool Q8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_kernel_dev(const Schedule<kSegCapLarge>* sched, const __grid_constant__ DecodeArgs a,
                       const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope) {
-  decode_body<GlobalSched, F8, true>(GlobalSched{sched}, a, tm_lat, tm_rope);
+  decode_body<GlobalSched, F8, true, Q8>(GlobalSched{sched}, a, tm_lat, tm_rope);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1116,14 +1129,14 @@ static bool make_map(CUtensorMap* m, const void* kv, int64_t rows, int box_cols,
   return r == CUDA_SUCCESS;
 }
 
-template <int CAP, bool F8>
+template <int CAP, bool F8, bool Q8>
 static cudaError_t launch_cap(const mla_plan& p, const DecodeArgs& a, const CUtensorMap& lat,
                               const CUtensorMap& rope, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err =
-        cudaFuncSetAttribute(decode_kernel<CAP, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncSetAttribute(decode_kernel<CAP, F8, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   Schedule<CAP> s;
@@ -1131,20 +1144,20 @@ static cudaError_t launch_cap(const mla_plan& p, const DecodeArgs& a, const CUte
   s.num_segments = (int32_t)p.segs.size();
   for (int w = 0; w <= p.num_workers; ++w) s.worker_seg[w] = p.worker_seg[w];
   for (size_t i = 0; i < p.segs.size(); ++i) s.seg[i] = p.segs[i];
-  decode_kernel<CAP, F8><<<dim3(2 * p.num_workers), kThreads, kSmemBytes, stream>>>(s, a, lat, rope);
+  decode_kernel<CAP, F8, Q8><<<dim3(2 * p.num_workers), kThreads, kSmemBytes, stream>>>(s, a, lat, rope);
   return cudaGetLastError();
 }
 
 // Device plan: the schedule sits at the head of the workspace, written by the
 // planner grid launched just before on the same stream; this launch is its
 // programmatic dependent (see decode_body).
-template <bool F8>
+template <bool F8, bool Q8>
 static cudaError_t launch_dev(const mla_plan& p, const DecodeArgs& a, const CUtensorMap& lat,
                               const CUtensorMap& rope, const void* workspace, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(decode_kernel_dev<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr_err = cudaFuncSetAttribute(decode_kernel_dev<F8, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const auto* sched = reinterpret_cast<const Schedule<kSegCapLarge>*>(static_cast<const char*>(workspace) +
@@ -1159,10 +1172,10 @@ static cudaError_t launch_dev(const mla_plan& p, const DecodeArgs& a, const CUte
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel_dev<F8>, sched, a, lat, rope);
+  return cudaLaunchKernelEx(&cfg, decode_kernel_dev<F8, Q8>, sched, a, lat, rope);
 }
 
-template <bool F8>
+template <bool F8, bool Q8>
 static cudaError_t launch_dtype(const mla_plan& p, const DecodeArgs& a, const void* workspace,
                                 cudaStream_t stream) {
   CUtensorMap lat, rope;
@@ -1175,9 +1188,9 @@ static cudaError_t launch_dtype(const mla_plan& p, const DecodeArgs& a, const vo
                      : make_map(&lat, a.kv, rows, 64, a.page_size, CU_TENSOR_MAP_SWIZZLE_128B, false) &&
                            make_map(&rope, a.kv, rows, 32, a.page_size, CU_TENSOR_MAP_SWIZZLE_64B, false);
   if (!ok) return cudaErrorNotSupported;
-  if (p.device) return launch_dev<F8>(p, a, lat, rope, workspace, stream);
-  if (p.segs.size() <= (size_t)kSegCapSmall) return launch_cap<kSegCapSmall, F8>(p, a, lat, rope, stream);
-  return launch_cap<kSegCapLarge, F8>(p, a, lat, rope, stream);
+  if (p.device) return launch_dev<F8, Q8>(p, a, lat, rope, workspace, stream);
+  if (p.segs.size() <= (size_t)kSegCapSmall) return launch_cap<kSegCapSmall, F8, Q8>(p, a, lat, rope, stream);
+  return launch_cap<kSegCapLarge, F8, Q8>(p, a, lat, rope, stream);
 }
 
 }  // namespace sm103
@@ -1185,8 +1198,10 @@ static cudaError_t launch_dtype(const mla_plan& p, const DecodeArgs& a, const vo
 // Returns cudaErrorNotSupported when the tensor-map encoder is unavailable.
 // `workspace` is read only for a device plan (its schedule area).
 cudaError_t launch_sm103(const mla_plan& p, const DecodeArgs& a, const void* workspace, cudaStream_t stream) {
-  return a.kv_dtype == MLA_KV_E4M3 ? sm103::launch_dtype<true>(p, a, workspace, stream)
-                                   : sm103::launch_dtype<false>(p, a, workspace, stream);
+  // the e4m3 query exists only with an e4m3 cache (the pages' FP8 path)
+  if (a.q_e4m3) return sm103::launch_dtype<true, true>(p, a, workspace, stream);
+  return a.kv_dtype == MLA_KV_E4M3 ? sm103::launch_dtype<true, false>(p, a, workspace, stream)
+                                   : sm103::launch_dtype<false, false>(p, a, workspace, stream);
 }
 
 // Kernel-side error code recorded since the last reset (0 = none).

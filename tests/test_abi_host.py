@@ -213,3 +213,19 @@ def test_ragged_plan_rules():
 def test_ragged_valid_args_reach_device_check(ragged_plan):
     no_gpu()
     assert call_ragged(ragged_plan) in (B.MLA_ERR_CUDA, B.MLA_ERR_UNSUPPORTED, B.MLA_OK)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), B.MLA_ERR_ARG), (dict(q=FAKE + 8), B.MLA_ERR_ARG), (dict(num_tokens=5), B.MLA_ERR_PLAN_MISMATCH),
+    (dict(num_heads=8), B.MLA_ERR_PLAN_MISMATCH), (dict(k_scale=0.0), B.MLA_ERR_ARG), (dict(ws=None), B.MLA_ERR_WORKSPACE),
+])
+def test_decode_fp8q_rejects(split_plan, over, code):
+    kw = dict(q=FAKE, num_tokens=split_plan.batch * split_plan.q_len, num_heads=split_plan.num_heads, kv=FAKE,
+              num_pages=100, page_size=split_plan.page_size, bt=FAKE, bt_stride=64, seq_lens=FAKE, cu=None,
+              scale=0.07, k_scale=1.0, out=FAKE, lse=FAKE, ws=FAKE, ws_bytes=split_plan.workspace_bytes)
+    kw.update(over)
+    rc = B.load().mla_decode_fp8q(split_plan.handle, kw["q"], kw["num_tokens"], kw["num_heads"], kw["kv"],
+                                  kw["num_pages"], kw["page_size"], kw["bt"], kw["bt_stride"], kw["seq_lens"],
+                                  kw["cu"], kw["scale"], kw["k_scale"], kw["out"], kw["lse"], kw["ws"],
+                                  kw["ws_bytes"], None)
+    assert rc == code
