@@ -10,9 +10,11 @@
 // MIN).
 // Request b's tiles occupy cost [P_b, P_b + n_b) (its overhead follows
 // them); worker w owns cost [w * cap, (w + 1) * cap).  The pieces of b are
-// its intersections with the worker intervals, except that a first or last
-// piece shorter than MIN tiles is merged into its neighbour piece.  A
-// request with no tile is one empty segment on the worker holding P_b.
+// its intersections with the worker intervals, whatever their length: each
+// piece pays the segment overhead on its worker, and merging a short piece
+// into a neighbour instead would load that neighbour past the capacity (a
+// request just longer than cap would land whole on one worker).  A request
+// with no tile is one empty segment on the worker holding P_b.
 // Requests and their pieces are emitted in order, so segments come out
 // sorted by worker.  Split requests (two or more pieces) take consecutive
 // partial slots and one combine job each; with every split spanning a worker
@@ -73,14 +75,6 @@ __device__ __forceinline__ Piece pieces_of(long long p, int n, long long cap, in
   long long w0 = p / cap, w1 = (p + n - 1) / cap;
   if (w1 > workers - 1) w1 = workers - 1;
   if (w0 > w1) w0 = w1;
-  if (w1 > w0) {
-    const long long first = (w0 + 1) * cap - p;
-    if (first < kMinSplitTiles) ++w0;
-  }
-  if (w1 > w0) {
-    const long long last = p + n - w1 * cap;
-    if (last < kMinSplitTiles) --w1;
-  }
   return Piece{(int)w0, (int)(w1 - w0 + 1)};
 }
 
@@ -107,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   long long total;
   long long p = block_exclusive_scan(cost, &total, s_warp);
-  // at least MIN, so that a middle piece (cap tiles) is never too short
+  // at least MIN tiles per worker interval
   long long cap = (total + workers - 1) / workers;
   cap = cap < kMinSplitTiles ? kMinSplitTiles : cap;
 
