@@ -312,7 +312,8 @@ int mla_plan_read_device_schedule(const mla_plan* plan, const void* workspace, i
  *   kv_pages, kv_dtype, num_pages, page_size  the cache as mla_decode takes
  *                 it; token t's row [k_nope | rope(k_rope)] is written at
  *                 slot out_cache_loc[t] (device int64 [num_tokens]): row
- *                 slot % page_size of page slot / page_size.
+ *                 slot % page_size of page slot / page_size.  Slots must be
+ *                 distinct (two tokens writing one slot race, as any scatter).
  * FP8 values are rounded to nearest (ties to even) and saturate at +-448,
  * with no scale (the pages pass none); bf16 values round to nearest even.
  * Device-side errors (mla_decode_device_error): a position outside
