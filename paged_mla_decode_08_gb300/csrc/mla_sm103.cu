@@ -828,34 +828,18 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
         mbar_arrive(c.bar(B_PAIR_MAX + 2 * quad + sb));
         if (!wait_bar_warp<false>(c, c.bar(B_PAIR_MAX + 2 * quad + sb), (j >> 1) & 1, 0x306)) { ok = false; break; }
         mt = fmaxf(red_max[(sb * 2) * 128 + row], red_max[(sb * 2 + 1) * 128 + row]) * cs;
-        // ---- O is idle once the previous tile's P.V is done
-        if (jj > 0) {
-          if (!wait_bar_warp<false>(c, c.bar(B_PV_DONE), (j - 1) & 1, 0x304)) { ok = false; break; }
-          tc_fence_after();
-        }
         // lazy rescale: the reference max moves only when it grew by more than
-        // 2^8; both halves decide identically; TMEM traffic by whole warps
+        // 2^8; both halves decide identically.  The decision and P need only
+        // S, so they are formed while the previous tile's P.V still runs.
         const float m_new = fmaxf(m_ref, mt);
         const bool resc = m_new > m_ref + kRescaleThreshold;
         const float alpha = resc ? ex2_approx(m_ref - m_new) : 1.f;  // 0 when m_ref = -inf
-        if (jj > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-          for (int ck = 0; ck < 4; ++ck) {
-            uint32_t o[32];
-            const uint32_t addr = tmem + lane_off + TM_O + 128 * half + 32 * ck;
-            tmem_ld32(addr, o);
-#pragma unroll
-            for (int v = 0; v < 32; ++v) o[v] = __float_as_uint(__uint_as_float(o[v]) * alpha);
-            tmem_st32(addr, o);
-          }
-        }
         if (resc) {
           l *= alpha;
           m_ref = m_new;
         }
         const float nm = m_ref == -CUDART_INF_F ? 0.f : -m_ref;  // all-masked rows: 2^-inf = 0
-        // ---- P (bf16 pairs) to shared memory, K-major 128B swizzle: this
-        // thread's 32 keys are 16-byte chunks 4*half..4*half+3 of its row
+        // ---- P as bf16 (fp16 for a float8 cache) pairs in registers
         uint32_t pk[16];
         float lsum = 0.f;
 #pragma unroll
@@ -872,8 +856,27 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
           lsum += p0 + p1;  // l from the unrounded probabilities: exact lse
         }
         l += lsum;
+        // ---- O and the P buffer are idle once the previous tile's P.V is
+        // done; a rescale of O is TMEM traffic by whole warps
+        if (jj > 0) {
+          if (!wait_bar_warp<false>(c, c.bar(B_PV_DONE), (j - 1) & 1, 0x304)) { ok = false; break; }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+            for (int ck = 0; ck < 4; ++ck) {
+              uint32_t o[32];
+              const uint32_t addr = tmem + lane_off + TM_O + 128 * half + 32 * ck;
+              tmem_ld32(addr, o);
+#pragma unroll
+              for (int v = 0; v < 32; ++v) o[v] = __float_as_uint(__uint_as_float(o[v]) * alpha);
+              tmem_st32(addr, o);
+            }
+          }
+        }
+        // ---- P to shared memory, K-major 128B swizzle: this thread's 32 keys
+        // are 16-byte chunks 4*half..4*half+3 of its row
         {
-          const uint32_t prow = c.sbase + OFF_P + row * 128;  // free: P.V of the previous tile is done
+          const uint32_t prow = c.sbase + OFF_P + row * 128;
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             st_shared_v4(prow + (((4 * half + i) ^ (row & 7)) << 4),
