@@ -56,11 +56,21 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text):
+    """Source text without comments and blank lines: what the compiled kernel
+    depends on, so a comment edit keeps the profiles that match the code."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash():
+    """sha256 (first 16 hex digits) of the main kernel's sources, comments and
+    blank lines removed."""
     h = hashlib.sha256()
     for f in MAIN_KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "paged_mla_decode_08_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_mla_decode_08_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

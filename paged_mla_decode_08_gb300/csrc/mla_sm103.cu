@@ -32,9 +32,10 @@
 // returns.
 //
 // Float8 (e4m3) cache.  The same kernel, instantiated with F8 = true: TMA
-// brings raw e4m3 tiles (half the bytes) into a 4-stage fp8 ring, the two
-// converter warps expand each tile into an fp16 operand stage laid out like
-// a bf16 stage (cvt.rn.f16x2.e4m3x2 is exact), and the MMAs run on fp16
+// brings raw e4m3 tiles (half the bytes) into a 2-stage fp8 ring, the two
+// converter warps expand each tile into one of 3 fp16 operand stages laid
+// out like a bf16 stage (cvt.rn.f16x2.e4m3x2 is exact; the two rings share
+// the bytes of the bf16 ring), and the MMAs run on fp16
 // operands (the query is converted to fp16 once per segment, P is packed
 // to fp16).  The per-tensor scale k_scale multiplies the scores and the
 // output (it is folded into the score scale and the epilogue scale).
