@@ -19,7 +19,7 @@
 // TMEM (512 columns): O [0,256), S double buffer [256,320) / [320,384), Q
 // latent half [384,512).  Shared memory: 4-stage cache-tile ring (36 KB per
 // stage), the rope half of Q (8 KB), the P tile (16 KB, the A operand of
-// P.V), a 3-slot ring of half-tile score-exchange buffers (16 KB each)
+// P.V), a 3-slot ring of half-tile score-exchange buffers (12 KB each)
 // written by the peer CTA.
 //
 // Warp roles (512 threads): warp 0 TMA producer, warp 1 TMEM allocator and
@@ -80,10 +80,13 @@ constexpr int OFF_QROPE = kStages * kStageBytes;       // 128 rows x 64 B
 constexpr int OFF_P = OFF_QROPE + 128 * 64;            // P (128 rows x 64 keys bf16, 128B swizzle)
 constexpr int kPBytes = 128 * 128;
 // Score exchange: a ring of 3 slots, each holding the peer's partial scores
-// of one half tile (32 keys) for 128 rows, [16-byte chunk][row] fp32.
+// of one half tile (32 keys) for 128 rows, [16-byte chunk][row], as 24-bit
+// codes (see score24).
 constexpr int kSlots = 3;
 constexpr int OFF_XCHG = OFF_P + kPBytes;
-constexpr int kSlotBytes = 128 * 32 * 4;
+constexpr int kXchgRowBytes = 32 * 3;  // 32 scores of 24 bits: six 16-byte chunks per row
+constexpr int kXchgChunks = kXchgRowBytes / 16;
+constexpr int kSlotBytes = 128 * kXchgRowBytes;
 constexpr int OFF_RED = OFF_XCHG + kSlots * kSlotBytes;  // row max / row sum exchange, 4 KB
 constexpr int OFF_SINK = OFF_RED + 4 * 2 * 128 * 4;      // per slot 128 words: the peer's "read done" notes
 constexpr int kNoteBytes = 128 * 4;
@@ -567,11 +570,28 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& rlo, fl
 
 // ------------------------------------------------------------------ exchange
 
+// Partial scores cross to the peer as 24-bit codes: the float's top 24 bits,
+// rounded to nearest on the 8 dropped mantissa bits (relative error 2^-16).
+// Four codes fill three words.
+__device__ __forceinline__ uint32_t score24(uint32_t bits) { return (bits + 0x80u) >> 8; }
+__device__ __forceinline__ void pack24(const uint32_t* v, uint32_t* w) {
+  const uint32_t a = score24(v[0]), b = score24(v[1]), c = score24(v[2]), d = score24(v[3]);
+  w[0] = a | (b << 24);
+  w[1] = (b >> 8) | (c << 16);
+  w[2] = (c >> 16) | (d << 8);
+}
+__device__ __forceinline__ void unpack24(const uint32_t* w, float* v) {
+  v[0] = __uint_as_float(w[0] << 8);
+  v[1] = __uint_as_float(((w[0] >> 24) | (w[1] << 8)) << 8);
+  v[2] = __uint_as_float(((w[1] >> 16) | (w[2] << 16)) << 8);
+  v[3] = __uint_as_float((w[2] >> 8) << 8);
+}
+
 // Warps 12-15 (one per TMEM lane quadrant, thread = query row): as soon as a
 // tile's partial scores land in TMEM, copy them to registers and stream them
 // into the peer CTA's receive buffer with st.async, which completes bytes on
 // the peer's x_full barrier.  Decoupled from the softmax warps so that the
-// ~0.5 us it takes to issue 32 KB of remote stores never blocks them.
+// time it takes to issue 24 KB of remote stores per tile never blocks them.
 // bf16 pair -> fp16 pair (exact for values in fp16's normal range, which
 // covers any sane query; used for the fp16 operands of the e4m3 path)
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
@@ -707,9 +727,12 @@ __device__ void exchanger(const Ctx& c, const S& sched, const DecodeArgs& a, uin
         const uint32_t mb = x_full_peer + 8 * k;
         const uint32_t* sv = sv64 + 32 * h;
         if (valid_row) {
+          uint32_t w[24];
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            st_async_v4(dst + ch * 2048, sv[4 * ch], sv[4 * ch + 1], sv[4 * ch + 2], sv[4 * ch + 3], mb);
+          for (int q = 0; q < 8; ++q) pack24(sv + 4 * q, w + 3 * q);
+#pragma unroll
+          for (int ch = 0; ch < kXchgChunks; ++ch)
+            st_async_v4(dst + ch * 2048, w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3], mb);
         }
         // arm the "peer has read it" phase of this slot: one 4-byte note per live row
         if (threadIdx.x == 384) mbar_arrive_expect_tx(c.bar(B_X_EMPTY + k), 4 * M);
@@ -788,20 +811,25 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
         // slot again before all "read" notes of this phase reached it.
         const int g = 2 * j + half, slot = g % kSlots, ug = g / kSlots;
         if (warp_live && !wait_bar_warp<true>(c, c.bar(B_X_FULL + slot), ug & 1, 0x303)) { ok = false; break; }
-        if (threadIdx.x == rearm_thread) mbar_arrive_expect_tx(c.bar(B_X_FULL + slot), 128 * M);  // row 0: live
+        if (threadIdx.x == rearm_thread) mbar_arrive_expect_tx(c.bar(B_X_FULL + slot), kXchgRowBytes * M);  // row 0: live
         float x[32];
         if (!warp_live) {
 #pragma unroll
           for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(cur[k]);  // masked below: no visible key
         } else {
           const uint32_t srcx = xchg_local + slot * kSlotBytes;
+          uint32_t w[24];
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
+          for (int ch = 0; ch < kXchgChunks; ++ch) {
             const uint4 v = ld_shared_v4(srcx + ch * 2048);
-            x[4 * ch + 0] = __uint_as_float(cur[4 * ch + 0]) + __uint_as_float(v.x);
-            x[4 * ch + 1] = __uint_as_float(cur[4 * ch + 1]) + __uint_as_float(v.y);
-            x[4 * ch + 2] = __uint_as_float(cur[4 * ch + 2]) + __uint_as_float(v.z);
-            x[4 * ch + 3] = __uint_as_float(cur[4 * ch + 3]) + __uint_as_float(v.w);
+            w[4 * ch + 0] = v.x; w[4 * ch + 1] = v.y; w[4 * ch + 2] = v.z; w[4 * ch + 3] = v.w;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float pv[4];
+            unpack24(w + 3 * q, pv);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) x[4 * q + t] = __uint_as_float(cur[4 * q + t]) + pv[t];
           }
         }
         // ---- causal / length mask (tail tiles only), row max over both
@@ -1038,7 +1066,7 @@ __device__ __forceinline__ void decode_body(const S& sched, const DecodeArgs& a,
     for (int i = 0; i < 8; ++i) mbar_init(c.bar(B_PAIR_MAX + i), 64);
     // receive buffers are armed one phase ahead: phase 0 now, phase u+1 as
     // soon as phase u completed (so the peer's bytes never precede the arm)
-    for (int k = 0; k < kSlots; ++k) mbar_arrive_expect_tx(c.bar(B_X_FULL + k), 128 * a.rows);
+    for (int k = 0; k < kSlots; ++k) mbar_arrive_expect_tx(c.bar(B_X_FULL + k), kXchgRowBytes * a.rows);
     for (int i = 0; i < 4; ++i) mbar_init(c.bar(B_PAIR_L + i), 64);
     for (int i = 0; i < 2; ++i) mbar_init(c.bar(B_S_LOADED + i), 128);
     for (int i = 0; i < 2; ++i) mbar_init(c.bar(B_S_FREE + i), 256);
