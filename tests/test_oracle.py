@@ -10,7 +10,6 @@ and checks that they are caught.
 import math
 
 import numpy as np
-import pytest
 import torch
 
 from oracle import mla_ref as O

@@ -3,8 +3,6 @@ documented rule, plus the coverage invariants any valid schedule must meet
 (each (request, tile) in exactly one segment, a request's segments contiguous
 and in order, one direct segment or consecutive partial slots)."""
 
-import math
-
 import numpy as np
 import pytest
 
