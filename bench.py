@@ -80,7 +80,8 @@ def profiled_traffic(config_name):
     path = os.path.join(ROOT, "profiles", f"mla_main_{config_name}_ncu.md")
     if not os.path.exists(path):
         return None
-    txt = open(path).read()
+    with open(path) as fh:
+        txt = fh.read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     hsh = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
     if not m or not hsh or hsh.group(1) != kernel_source_hash():
