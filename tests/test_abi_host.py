@@ -230,3 +230,10 @@ def test_decode_fp8q_rejects(split_plan, over, code):
                                   kw["cu"], kw["scale"], kw["k_scale"], kw["out"], kw["lse"], kw["ws"],
                                   kw["ws_bytes"], None)
     assert rc == code
+
+
+def test_binding_refuses_a_missing_library(tmp_path):
+    """The product path has no fallback: a missing shared library is an error."""
+    missing = str(tmp_path / "libmladecode.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        B.load(missing)
