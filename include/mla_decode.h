@@ -38,6 +38,17 @@
  *   - Nothing in mla_decode allocates, frees or synchronises; all argument
  *     errors are detected on the host before any launch.
  *   - bf16 values are IEEE bfloat16, e4m3 values are OCP float8 e4m3fn.
+ *
+ * Precision.  Products run on the tensor cores with bf16 operands (fp16 for
+ * an e4m3 cache, to which e4m3 and a bf16 query convert exactly) and fp32
+ * accumulation.  Each score is the sum of two fp32 partial products, one of
+ * which is rounded to 24 bits (relative error at most 2^-16) on its way
+ * between the two CTAs that share the work.  Probabilities enter P.V as bf16
+ * (fp16 for an e4m3 cache); the row sums and the lse use them unrounded.
+ * Split requests merge bf16 partial outputs.  Against the exact float64
+ * result the library is tested to max|out - ref| <= 1e-2 * max|ref| + 1e-3
+ * and |lse - ref| <= 2e-3 (bf16 cache), and max|out - ref| <= 5e-2 * max|ref|
+ * (e4m3 cache); rows with no visible key are exactly 0 and -inf.
  */
 #ifndef MLA_DECODE_H_
 #define MLA_DECODE_H_
