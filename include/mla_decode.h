@@ -330,7 +330,9 @@ int mla_plan_read_device_schedule(const mla_plan* plan, const void* workspace, i
  * Device-side errors (mla_decode_device_error): a position outside
  * [0, max_position) leaves that token's outputs unwritten (0x601); a slot
  * outside the cache leaves its key row unwritten (0x602).  Host-side:
- * MLA_ERR_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA.
+ * MLA_ERR_ARG (also when num_tokens * (num_heads + 1) * 72 exceeds the
+ * (2^31 - 1) * 256 items one launch covers), MLA_ERR_UNSUPPORTED,
+ * MLA_ERR_CUDA.
  */
 #define MLA_Q_BF16 0
 #define MLA_Q_E4M3 1

@@ -434,7 +434,9 @@ int mla_rope_quantize_cache_write(const void* q_nope, const void* q_rope, int nu
                                   int is_neox, void* kv_pages, int kv_dtype, int64_t num_pages, int page_size,
                                   const int64_t* out_cache_loc, void* stream) {
   if (num_tokens < 1 || num_heads < 0 || num_heads > (1 << 16)) return fail(MLA_ERR_ARG, "num_tokens >= 1, num_heads in [0, 65536]");
-  if ((int64_t)num_tokens * (num_heads + 1) * 72 > ((int64_t)1 << 40)) return fail(MLA_ERR_ARG, "too many tokens");
+  // one flat grid of 256-thread blocks covers 72 items per (token, head or key) row
+  if ((int64_t)num_tokens * (num_heads + 1) * 72 > (int64_t)INT32_MAX * 256)
+    return fail(MLA_ERR_ARG, "too many tokens x heads for one launch");
   if (q_out_dtype != MLA_Q_BF16 && q_out_dtype != MLA_Q_E4M3) return fail(MLA_ERR_ARG, "q_out_dtype must be MLA_Q_BF16 or MLA_Q_E4M3");
   if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_E4M3) return fail(MLA_ERR_ARG, "kv_dtype must be MLA_KV_BF16 or MLA_KV_E4M3");
   if (page_size != 32 && page_size != 64) return fail(MLA_ERR_ARG, "page_size must be 32 or 64");

@@ -237,3 +237,37 @@ def test_binding_refuses_a_missing_library(tmp_path):
     missing = str(tmp_path / "libmladecode.so")
     with pytest.raises(RuntimeError, match="not built"):
         B.load(missing)
+
+
+def call_rope_write(**over):
+    kw = dict(q_nope=FAKE, q_rope=FAKE, num_tokens=4, num_heads=8, q_out=FAKE, q_out_dtype=B.MLA_Q_E4M3,
+              k_nope=FAKE, k_rope=FAKE, positions=FAKE, cos_sin=FAKE, max_position=4096, is_neox=0,
+              kv=FAKE, kv_dtype=B.MLA_KV_E4M3, num_pages=64, page_size=64, slots=FAKE, stream=None)
+    kw.update(over)
+    return B.load().mla_rope_quantize_cache_write(
+        kw["q_nope"], kw["q_rope"], kw["num_tokens"], kw["num_heads"], kw["q_out"], kw["q_out_dtype"],
+        kw["k_nope"], kw["k_rope"], kw["positions"], kw["cos_sin"], kw["max_position"], kw["is_neox"],
+        kw["kv"], kw["kv_dtype"], kw["num_pages"], kw["page_size"], kw["slots"], kw["stream"])
+
+
+@pytest.mark.parametrize("over", [
+    dict(num_tokens=0), dict(num_heads=-1), dict(num_heads=(1 << 16) + 1),
+    dict(num_tokens=1 << 30, num_heads=1 << 16),               # more items than one grid covers
+    dict(q_out_dtype=7), dict(kv_dtype=5), dict(page_size=16), dict(num_pages=0), dict(num_pages=1 << 40),
+    dict(k_nope=None), dict(k_rope=None), dict(kv=None), dict(slots=None),
+    dict(q_rope=None), dict(q_out=None), dict(q_nope=None),   # the e4m3 query needs its latent part
+    dict(positions=None), dict(max_position=0),               # a table needs positions
+    dict(k_nope=FAKE + 8), dict(kv=FAKE + 4), dict(slots=FAKE + 4), dict(cos_sin=FAKE + 4), dict(q_out=FAKE + 8),
+])
+def test_rope_cache_write_rejects(over):
+    assert call_rope_write(**over) == B.MLA_ERR_ARG
+
+
+def test_rope_cache_write_valid_args_reach_device_check():
+    no_gpu()
+    ok = (B.MLA_ERR_CUDA, B.MLA_ERR_UNSUPPORTED, B.MLA_OK)
+    assert call_rope_write() in ok
+    # a plain cache write: no query at all, and no rotation table
+    assert call_rope_write(num_heads=0, q_nope=None, q_rope=None, q_out=None, cos_sin=None, positions=None) in ok
+    # a bf16 q_pe output needs no latent query input
+    assert call_rope_write(q_out_dtype=B.MLA_Q_BF16, q_nope=None, kv_dtype=B.MLA_KV_BF16) in ok
