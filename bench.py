@@ -1,7 +1,9 @@
 """Decode benchmark: weight-absorbed paged MLA decode on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config dsv3|tiny|long_skewed|spec_q4|fp8_kv]
+                    [--config dsv3|tiny|long_skewed|spec_q4|fp8_kv] [--seed S]
+                    [--soak SECONDS] [--cpu-seconds SECONDS]
+                    [--profile [--pool-pages P]]
 
 A step is one whole decode (split-KV main kernel + LSE combine) over one
 resident batch of the DeepSeek-V3-shaped workload (B=64 requests, q_len=1,
@@ -575,9 +577,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="dsv3", choices=list(W.CONFIGS))
-    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--seed", type=int, default=0, help="workload seed (rank r draws seed + r)")
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed steps before timing")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="host time for the cpu_baseline sample of the oracle")
     ap.add_argument("--profile", action="store_true",
                     help="run --warmup + 1 decode steps of --config and exit: a small, fixed launch sequence "
                          "for ncu captures (no timing, no JSON line)")
