@@ -9,7 +9,8 @@
 //   S_r = Q[:, half r] . KV[:, half r]^T    (M = 128 query rows, N = 64 keys,
 //                                           K = 256 + 32)      -> TMEM
 //   S   = S_0 + S_1                         (partial scores swapped through
-//                                           distributed shared memory)
+//                                           distributed shared memory as
+//                                           24-bit codes, see score24)
 //   P   = exp2(S * scale*log2e - m)         (both CTAs compute the same P)
 //   O_r += P . c_kv[:, half r]              (M = 128, N = 256, K = 64) -> TMEM
 // The cache tile in shared memory serves both products: K-major as the B
