@@ -2,14 +2,18 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--config dsv3|tiny|long_skewed|spec_q4|fp8_kv] [--seed S]
-                    [--soak SECONDS] [--cpu-seconds SECONDS]
+                    [--soak SECONDS] [--cpu-seconds SECONDS] [--configs all|none|a,b]
                     [--profile [--pool-pages P]]
 
 A step is one whole decode (split-KV main kernel + LSE combine) over one
 resident batch of the DeepSeek-V3-shaped workload (B=64 requests, q_len=1,
 H=128, kv_lora_rank 512 + rope 64, L ~ U[1024, 4096], page 64, shuffled
 16384-page pool, seed 0).  L2 is flushed (a write of 2x the L2 size) between
-steps, outside the timed events.  Rank 0 prints one JSON line.
+steps, outside the timed events.  Rank 0 prints one JSON line; its
+``configs`` object holds the same measurement for every other seeded
+workload (tiny, long_skewed, spec_q4, fp8_kv), each with the roofline of its
+main kernel, and ``host_plan_us`` / ``e2e_replan`` the cost of planning on
+the host from the lengths of every step.
 
 --impl reference times the float64 CPU oracle (the only reference this
 decode has) on the host cores, same workload and metric.
@@ -322,22 +326,27 @@ def our_arm(args, w, rank, world):
     devplan = device_plan_measure(db, w, dev, stream, flush, max(3, min(K, 200)), st)
     # ---- the step before: RoPE + FP8 quantisation + cache write of the new tokens
     rope_write = rope_write_measure(w, dev, stream, flush, max(3, min(K, 200)), peaks)
+    # ---- a serving step that re-plans on the host from the new lengths
+    e2e_rp = e2e_replan_measure(db, w, dev, stream, max(3, min(K, 200)))
+    plan_us = host_plan_us(w)
+    # ---- every other seeded workload, timed the same way
+    names = [] if args.configs == "none" else (
+        list(W.CONFIGS) if args.configs == "all" else [n for n in args.configs.split(",") if n])
+    per_config = {}
+    for name in names:
+        if name == w.name:
+            continue
+        per_config[name] = config_measure(name, args.seed + rank, dev, stream, flush, max(3, min(K, 100)), peaks,
+                                          peaks_kind)
 
     if rank != 0:
         return
     main_avg_s = statistics.mean(main_ms) / 1e3
     step_avg_s = statistics.mean(step_ms) / 1e3
-    hbm_peak = float(peaks["hbm_gbs"])
-    tc_peak = float(peaks["bf16_tflops"])
-    t_hbm = st["alg_bytes"] / (hbm_peak * 1e9)
-    t_tc = st["flops"] / (tc_peak * 1e12)
-    bound = "hbm" if t_hbm >= t_tc else "tensor"
-    if bound == "hbm":
-        achieved = st["alg_bytes"] / main_avg_s / 1e9
-        peak, unit = hbm_peak, "GB/s"
-    else:
-        achieved = st["flops"] / main_avg_s / 1e12
-        peak, unit = tc_peak, "TFLOP/s"
+    t_hbm = st["alg_bytes"] / (float(peaks["hbm_gbs"]) * 1e9)
+    t_tc = st["flops"] / (float(peaks["bf16_tflops"]) * 1e12)
+    rl = roofline_of(st, main_avg_s, peaks, peaks_kind, "bf16" if w.kv_dtype == "bf16" else "fp16")
+    bound, achieved, peak, unit = rl["bound"], rl["achieved"], rl["peak"], rl["unit"]
     cpu_v, cpu_el, cpu_rows = time_oracle(w, budget_s=args.cpu_seconds)
     clocks = ClockSampler.summarize(clock_rows, peaks)
     line = {
@@ -368,9 +377,127 @@ def our_arm(args, w, rank, world):
         "device_plan": devplan,
         "rope_quantize_write": rope_write,
         "segments": int(len(db.plan.segments())), "partial_slots": db.plan.num_partial_slots,
+        "host_plan_us": plan_us,
+        "e2e_replan": e2e_rp,
         "kernel_source_sha": kernel_source_hash(),
+        "configs": per_config,
     }
     print(json.dumps(line), flush=True)
+
+
+def roofline_of(st, main_s, peaks, peaks_kind, mma="bf16"):
+    """Roofline of one main-kernel launch: the slower of the algorithmic
+    bytes at the HBM peak and the algorithmic flops at the tensor peak of the
+    MMA precision used (bf16 and fp16 MMAs share the measured bf16 rate)."""
+    hbm_peak = float(peaks["hbm_gbs"])
+    tc_peak = float(peaks["bf16_tflops"])
+    t_hbm = st["alg_bytes"] / (hbm_peak * 1e9)
+    t_tc = st["flops"] / (tc_peak * 1e12)
+    if t_hbm >= t_tc:
+        achieved, peak, unit, bound = st["alg_bytes"] / main_s / 1e9, hbm_peak, "GB/s", "hbm"
+    else:
+        achieved, peak, unit, bound = st["flops"] / main_s / 1e12, tc_peak, "TFLOP/s", "tensor"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "peak_kind": peaks_kind, "mma": mma, "t_roof_us": max(t_hbm, t_tc) * 1e6,
+            "alg_bytes_per_launch": st["alg_bytes"], "alg_flops_per_launch": st["flops"]}
+
+
+def config_measure(name, seed, dev, stream, flush, K, peaks, peaks_kind):
+    """One seeded workload timed like the headline step: K decode steps
+    (main kernel + combine, L2 flushed before each, events on the launching
+    stream), then K steps with an event between the two launches for the
+    main kernel's own time; host plan cost; roofline of the main kernel."""
+    import torch
+    from paged_mla_decode_08_gb300 import runner as R
+    w = W.make_workload(name, seed=seed)
+    st = W.workload_stats(w)
+    db = R.upload(w, device=dev)
+    for _ in range(3):
+        flush.zero_()
+        R.decode(db, stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        R.decode(db, stream)
+        ev[k][1].record(stream)
+    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for k in range(K):
+        flush.zero_()
+        evk[k][0].record(stream)
+        R.decode_main(db, stream)
+        evk[k][1].record(stream)
+        R.decode_combine(db, stream)
+        evk[k][2].record(stream)
+    torch.cuda.synchronize()
+    step_s = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    main_s = statistics.mean(e[0].elapsed_time(e[1]) for e in evk) / 1e3
+    comb_us = statistics.mean(e[1].elapsed_time(e[2]) for e in evk) * 1e3
+    res = {
+        "workload": workload_desc(w)["workload"], "tokens_per_s": st["tokens"] / step_s,
+        "step_us": step_s * 1e6, "main_us": main_s * 1e6, "combine_us": comb_us,
+        "kv_gbs": st["kv_bytes"] / step_s / 1e9, "tflops": st["flops"] / step_s / 1e12,
+        "roofline": roofline_of(st, main_s, peaks, peaks_kind, "bf16" if w.kv_dtype == "bf16" else "fp16"),
+        "step_roofline_frac": roofline_of(st, step_s, peaks, peaks_kind)["frac"],
+        "host_plan_us": host_plan_us(w), "segments": int(len(db.plan.segments())),
+        "partial_slots": db.plan.num_partial_slots, "steps": K, "launches_per_step": 1 + (db.plan.num_partial_slots > 0),
+        "kernel_source_sha": kernel_source_hash(),
+    }
+    del db
+    torch.cuda.empty_cache()
+    return res
+
+
+def host_plan_us(w, reps=200):
+    """Mean wall time of one mla_decode_plan call from the host lengths
+    (through the Python binding, plan object freed each time)."""
+    from paged_mla_decode_08_gb300 import binding as B
+    lens = np.ascontiguousarray(w.seq_lens, dtype=np.int32)
+    B.mla_decode_plan(lens, w.page_size, w.num_heads, w.q_len)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        p = B.mla_decode_plan(lens, w.page_size, w.num_heads, w.q_len)
+        del p
+    return (time.perf_counter() - t0) / reps * 1e6
+
+
+def e2e_replan_measure(db, w, dev, stream, K):
+    """The e2e step of a host-planned serving loop: every step makes a new
+    plan from the host lengths, then copies the query, block table and
+    lengths in, decodes, and reads out and lse back (host-synchronous)."""
+    import torch
+    from paged_mla_decode_08_gb300 import binding as B
+    hq = db.q_nope.cpu().pin_memory()
+    hp = db.q_pe.cpu().pin_memory()
+    hbt = db.block_table.cpu().pin_memory()
+    hsl = db.seq_lens.cpu().pin_memory()
+    lens = np.ascontiguousarray(w.seq_lens, dtype=np.int32)
+    ho = torch.empty(db.out.shape, dtype=db.out.dtype).pin_memory()
+    hl = torch.empty(db.lse.shape, dtype=db.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hp, hbt, hsl))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl))
+
+    def one():
+        plan = B.mla_decode_plan(lens, w.page_size, w.num_heads, w.q_len)
+        db.q_nope.copy_(hq, non_blocking=True)
+        db.q_pe.copy_(hp, non_blocking=True)
+        db.block_table.copy_(hbt, non_blocking=True)
+        db.seq_lens.copy_(hsl, non_blocking=True)
+        B.mla_decode(plan, db.q_nope, db.q_pe, db.kv, db.kv_dtype, db.block_table, db.seq_lens, w.scale,
+                     w.k_scale, db.out, db.lse, db.workspace, None, stream)
+        ho.copy_(db.out, non_blocking=True)
+        hl.copy_(db.lse, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    for _ in range(3):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        one()
+    el = time.perf_counter() - t0
+    return {"value": w.num_tokens * K / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K,
+            "note": "host plan made from the host lengths inside every step; otherwise as e2e"}
 
 
 def block_table_measure(w, dev, stream, flush, K):
@@ -581,6 +708,9 @@ def main():
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed steps before timing")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="host time for the cpu_baseline sample of the oracle")
+    ap.add_argument("--configs", default="all",
+                    help="seeded workloads measured besides the headline one, into the line's 'configs' object: "
+                         "'all' (default), 'none', or a comma-separated list of names")
     ap.add_argument("--profile", action="store_true",
                     help="run --warmup + 1 decode steps of --config and exit: a small, fixed launch sequence "
                          "for ncu captures (no timing, no JSON line)")

@@ -247,8 +247,14 @@ int mla_decode_fp8q(const mla_plan* plan, const void* q, int num_tokens, int num
  *   - There is one array per device, shared by all calls on it; contents left
  *     by a previous call are never read before being rewritten, so nothing
  *     needs clearing, but calls that overlap on the GPU race: order them.
- *   - The first call on a device looks up the array's device address once;
- *     make that call before any stream capture.
+ *   - The array's device address is looked up (cudaGetSymbolAddress) the
+ *     first time a call runs under a CUDA context, and cached under that
+ *     context's unique id; a context made after cudaDeviceReset, or another
+ *     context, looks it up again.  That first call may load the library's
+ *     module in the context: make it before any stream capture.
+ *   - Errors: those of mla_decode (MLA_ERR_UNSUPPORTED on a device that is
+ *     not sm_103, checked before anything else); MLA_ERR_WORKSPACE for a
+ *     plan larger than the array; MLA_ERR_CUDA if the address lookup fails.
  */
 #define MLA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int mla_decode_noalloc(const mla_plan* plan, const void* q_nope, const void* q_pe, int num_tokens,

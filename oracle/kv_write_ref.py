@@ -36,7 +36,10 @@ and ``rotate_f32`` against within float32 rounding.
 parity pinned: tests/test_kv_write_oracle.py (hand-computed rotations, norm
 and relative-position properties of the rotation built from a RoFormer
 frequency table, both pairings, e4m3 rounding against the format table and
-torch, slot round trip through the decode's gather).
+torch, bf16 rounding against exact midpoints, signed zeros, the overflow
+boundary and torch's own cast, the bf16 rope output against exact quarter
+and half turns and against a float32 rotation done in torch, slot round trip
+through the decode's gather).
 """
 
 from __future__ import annotations
@@ -124,9 +127,20 @@ def rope_quantize_fp8(q_nope_bits, q_rope_bits, k_nope_bits, k_rope_bits, positi
 
 
 def round_bf16(x) -> np.ndarray:
-    """float32 values -> bf16 bit patterns, nearest even (finite inputs)."""
+    """float32 values -> bf16 bit patterns, round to nearest, ties to even
+    (the IEEE 754 default, which bf16 -- float32's top 16 bits -- inherits).
+
+    On the bit pattern u: the kept half is u >> 16; the dropped half is
+    compared with 0x8000 by adding 0x7FFF plus the kept half's lowest bit, so
+    a carry happens above the midpoint, and at the midpoint only when the kept
+    half is odd.  A carry out of the mantissa moves the exponent up, which is
+    also how the largest finite values overflow to infinity.  Infinities are
+    unchanged by this; NaN is handled apart (a quiet NaN of the same sign), as
+    the carry could turn a NaN into an infinity."""
     u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    nan = (u & 0x7FFFFFFF) > 0x7F800000
     u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    u = np.where(nan, ((np.ascontiguousarray(x, dtype=np.float32).view(np.uint32) >> 16) | 0x0040), u)
     return u.astype(np.uint16)
 
 

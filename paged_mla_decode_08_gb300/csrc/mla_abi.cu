@@ -164,6 +164,9 @@ int launch_combine(const mla_plan* plan, const Prepared& pr, cudaStream_t stream
 namespace mla {
 // Lets other translation units of the library record a failure message.
 int report_error(int code, const char* msg) { return fail(code, msg); }
+// The device check every entry point makes (sm_103 only), for other
+// translation units.
+int require_sm103() { return check_device(nullptr); }
 }  // namespace mla
 
 extern "C" {

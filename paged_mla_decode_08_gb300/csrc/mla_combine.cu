@@ -4,7 +4,8 @@
 // O_s = (sum_j p_j c_kv_j) / l_s (already scaled by the value
 // dequantisation factor) and lse_s.  The merge is
 //     lse = ln sum_s e^{lse_s},   out = sum_s e^{lse_s - lse} O_s,
-// where a split that saw no visible key has lse_s = -inf and weighs nothing;
+// where a split that saw no visible key has lse_s = -inf and weighs nothing
+// (a split with lse_s = NaN makes the row NaN, as the definition does);
 // if every split is empty the row is out = 0, lse = -inf, as the zero-KV rows
 // of the pages (sglang trtllm_mla_backend.py, forward_extend: fixed-up rows
 // with lse = -inf so the merge ignores them).
@@ -35,6 +36,12 @@ constexpr int kCombChunks = kChunks / 4;       // per CTA: a quarter of the row
 
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+// max(a, b), NaN if either is NaN
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
 
 // One (job, 32-row block, quarter of the columns) of the merge; called after
 // the grid dependency wait.
@@ -67,18 +74,21 @@ __device__ __forceinline__ void combine_body(const CombineJob job, const DecodeA
       v[g][k] = (r < nrows && g < job.nsplit) ? __ldg(po + g * split_stride + (size_t)(8 * k) * M) : make_uint4(0, 0, 0, 0);
 
   if (threadIdx.x < kCombRows) {
+    // A split with lse = NaN (a NaN score in its keys) makes the row NaN, as
+    // in the definition: the maximum propagates NaN (max.NaN), and from it
+    // the sum, the lse and every weight.
     float mx = -CUDART_INF_F, tot = 0.f;
     const float* pl = a.part_lse + (size_t)job.slot_begin * M + r0 + r;
     if (r < nrows) {
-      for (int s = 0; s < job.nsplit; ++s) mx = fmaxf(mx, __ldg(pl + (size_t)s * M));
+      for (int s = 0; s < job.nsplit; ++s) mx = max_nan(mx, __ldg(pl + (size_t)s * M));
       if (mx != -CUDART_INF_F)
         for (int s = 0; s < job.nsplit; ++s) tot += __expf(__ldg(pl + (size_t)s * M) - mx);
-      if (blockIdx.z == 0) a.lse[orow0 + r] = tot > 0.f ? mx + __logf(tot) : -CUDART_INF_F;
+      if (blockIdx.z == 0) a.lse[orow0 + r] = tot == 0.f ? -CUDART_INF_F : mx + __logf(tot);
     }
-    const float inv = tot > 0.f ? 1.f / tot : 0.f;
+    const float inv = tot == 0.f ? 0.f : 1.f / tot;
     for (int s = 0; s < job.nsplit; ++s) {
       const float l = r < nrows ? __ldg(pl + (size_t)s * M) : -CUDART_INF_F;
-      s_w[s * kCombRows + r] = (inv > 0.f && l != -CUDART_INF_F) ? __expf(l - mx) * inv : 0.f;
+      s_w[s * kCombRows + r] = (tot == 0.f || l == -CUDART_INF_F) ? 0.f : __expf(l - mx) * inv;
     }
   }
   __syncthreads();

@@ -573,8 +573,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& rlo, fl
 
 // Partial scores cross to the peer as 24-bit codes: the float's top 24 bits,
 // rounded to nearest on the 8 dropped mantissa bits (relative error 2^-16).
-// Four codes fill three words.
-__device__ __forceinline__ uint32_t score24(uint32_t bits) { return (bits + 0x80u) >> 8; }
+// Infinities and NaN (exponent all ones) are truncated instead, with the
+// lowest code bit set for a NaN whose payload sits in the dropped bits:
+// rounding could carry a NaN's mantissa into the sign bit, truncation alone
+// could turn such a NaN into an infinity, and the peer must see the same
+// non-finite score as this CTA.  Four codes fill three words.
+__device__ __forceinline__ uint32_t score24(uint32_t bits) {
+  if ((bits & 0x7F800000u) == 0x7F800000u) return (bits >> 8) | ((bits & 0x007FFFFFu) != 0u ? 1u : 0u);
+  return (bits + 0x80u) >> 8;
+}
 __device__ __forceinline__ void pack24(const uint32_t* v, uint32_t* w) {
   const uint32_t a = score24(v[0]), b = score24(v[1]), c = score24(v[2]), d = score24(v[3]);
   w[0] = a | (b << 24);
@@ -937,7 +944,10 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
       // (re-read from the cache: nothing is held across the tile loop)
       const int orow = out_row(seg_q(c, sched, a, s), a.num_heads, row);
       const bool live_row = orow >= 0;
-      const bool live = l > 0.f;
+      // l = 0 only for a row that saw no key; a NaN score (NaN in a visible
+      // cache row or in the query) leaves l NaN and the row NaN, as in the
+      // definition
+      const bool live = !(l == 0.f);
       const float inv = live ? a.out_scale / l : 0.f;
 #pragma unroll 1
       for (int ck = 0; ck < 4; ++ck) {

@@ -22,11 +22,17 @@ SCALE = 1.0 / np.sqrt(192.0)
 LATENT, ROPE = 512, 64
 
 
-def to_24bit(x32):
+def to_24bit(x32, guard=True):
     """float32 -> float32 keeping the top 24 bits, rounded to nearest on the
-    dropped 8 (the exchange code, restated)."""
-    bits = x32.astype(np.float32).view(np.uint32).astype(np.uint64)
+    dropped 8 (the exchange code, restated).  Infinities and NaN (exponent all
+    ones) are truncated instead of rounded, and a NaN keeps a non-zero
+    mantissa (the lowest code bit is set when the payload was non-zero);
+    ``guard=False`` restates the code without that exception."""
+    bits = np.asarray(x32, dtype=np.float32).view(np.uint32).astype(np.uint64)
     code = ((bits + 0x80) & 0xFFFFFFFF) >> 8
+    if guard:
+        special = (bits >> 8) | ((bits & 0x007FFFFF) != 0).astype(np.uint64)
+        code = np.where((bits & 0x7F800000) == 0x7F800000, special, code)
     return ((code << 8) & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
 
 
@@ -86,3 +92,29 @@ def test_fp16_exchange_would_break_the_bound_on_sharp_rows():
     assert np.abs(half - exact).max() > 2e-3
     assert np.abs(code24 - exact).max() <= 2.0 ** -16 * SCALE * np.abs(s1).max() * 1.01
     assert np.abs(code24 - exact).max() < 2e-3
+
+
+def test_non_finite_scores_cross_unchanged():
+    """An infinite partial stays that infinity and a NaN stays NaN (with its
+    sign), so both CTAs of the pair see the same non-finite score.  Rounding
+    them like finite values would not: the canonical NaN 0x7FFFFFFF carries
+    into the sign bit and arrives as -0.0, and a negative NaN wraps to +0."""
+    bits = np.array([0x7F800000, 0xFF800000, 0x7FFFFFFF, 0xFFFFFFFF, 0x7FC00000, 0x7F800001, 0xFF800080,
+                     0x7F7FFFFF], dtype=np.uint32)
+    x = bits.view(np.float32)
+    y = to_24bit(x)
+    assert y[0] == np.inf and y[1] == -np.inf
+    assert np.all(np.isnan(y[2:7]))
+    assert np.array_equal(np.signbit(y[2:7]), np.signbit(x[2:7]))
+    # the largest finite value rounds up to infinity, as round-to-nearest does
+    assert y[7] == np.inf
+    bad = to_24bit(x, guard=False)
+    assert bad[2] == 0.0 and np.signbit(bad[2]) and bad[3] == 0.0  # what the guard prevents
+    # a NaN whose payload is only in the dropped bits would become infinite
+    # if it were truncated without keeping a payload bit
+    trunc = ((bits.astype(np.uint64) >> 8) << 8).astype(np.uint32).view(np.float32)
+    assert np.isinf(trunc[5]) and np.isnan(y[5])
+    # finite values are untouched by the guard
+    rng = np.random.default_rng(3)
+    f = (rng.standard_normal(10000) * 10.0 ** rng.uniform(-30, 30, 10000)).astype(np.float32)
+    assert np.array_equal(to_24bit(f).view(np.uint32), to_24bit(f, guard=False).view(np.uint32))

@@ -8,7 +8,8 @@ rounding against the format's value table, its ties and saturation, and
 against torch's float8 conversion; the cache write round-trips through the
 decode oracle's gather.  ``test_planted_mistake_is_caught`` plants plausible
 mistakes (swapped sin sign, pairing swapped, truncation, ties away from zero,
-slot split by the wrong page size) and checks that a pin rejects each.
+the same four in bf16 rounding, NaN overflowing to infinity, slot split by the
+wrong page size) and checks that a pin rejects each.
 """
 
 import inspect
@@ -137,10 +138,110 @@ def pin_f32_tracks_f64(mod):
     return ok
 
 
+def _bf16_of_float32_bits(u32):
+    return np.asarray(u32, dtype=np.uint32).view(np.float32)
+
+
+def pin_bf16_rounding(mod):
+    """round_bf16 at the places that fix round-to-nearest-even: every exact
+    midpoint goes to the even neighbour (so odd kept halves round up, even
+    ones down), one unit above / below a midpoint goes to the nearer value,
+    signed zeros and infinities are kept, the largest finite values overflow
+    to infinity exactly at the midpoint past the bf16 maximum, and NaN stays
+    NaN."""
+    rng = np.random.default_rng(11)
+    hi = rng.integers(0, 0x7F80, size=4000).astype(np.uint32)  # finite kept halves, both parities
+    hi = np.concatenate([hi, hi | 0x8000, np.array([0, 1, 0x7F7E, 0x7F7F, 0x8000, 0x8001, 0xFF7F], np.uint32)])
+    even_up = hi + (hi & 1)  # ties to even: odd kept halves carry
+    ok = np.array_equal(mod.round_bf16(_bf16_of_float32_bits((hi << 16) | 0x8000)), even_up.astype(np.uint16))
+    ok &= np.array_equal(mod.round_bf16(_bf16_of_float32_bits((hi << 16) | 0x8001)), (hi + 1).astype(np.uint16))
+    ok &= np.array_equal(mod.round_bf16(_bf16_of_float32_bits((hi << 16) | 0x7FFF)), hi.astype(np.uint16))
+    ok &= np.array_equal(mod.round_bf16(_bf16_of_float32_bits(hi << 16)), hi.astype(np.uint16))
+    special = np.array([0x00000000, 0x80000000, 0x00000001, 0x00008000, 0x00018000, 0x7F7F7FFF, 0x7F7F8000,
+                        0xFF7F8000, 0x7F800000, 0xFF800000], dtype=np.uint32)
+    want = np.array([0x0000, 0x8000, 0x0000, 0x0000, 0x0002, 0x7F7F, 0x7F80, 0xFF80, 0x7F80, 0xFF80], np.uint16)
+    ok &= np.array_equal(mod.round_bf16(_bf16_of_float32_bits(special)), want)
+    nan = mod.round_bf16(_bf16_of_float32_bits(np.array([0x7F800001, 0xFF800001, 0x7FC00000, 0x7FFFFFFF],
+                                                         dtype=np.uint32)))
+    ok &= bool(np.all((nan & 0x7F80) == 0x7F80) and np.all((nan & 0x007F) != 0))  # NaN, not infinity
+    return bool(ok)
+
+
+def pin_bf16_against_torch(mod):
+    """Finite float32 values over the whole range, subnormals included: the
+    same bf16 bits as torch's own float32 -> bfloat16 cast."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal(60000) * 10.0 ** rng.uniform(-44, 38.5, 60000)
+    x = x[np.abs(x) < 3.0e38].astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return np.array_equal(mod.round_bf16(x), want)
+
+
+def pin_rope_bf16_quarter_turns(mod):
+    """rope_bf16 where the rotation is exact (quarter and half turns: a swap
+    and sign changes of bf16 values), for both pairings: the output bits are
+    the input's, moved and negated as worked out by hand."""
+    rng = np.random.default_rng(13)
+    x_bits = W_bits(rng.standard_normal(64).astype(np.float32))
+    x = O.decode_bf16(x_bits)
+    cs = np.zeros((3, 64), dtype=np.float32)
+    cs[:, :32] = 1.0                       # position 0: identity
+    cs[1, 0], cs[1, 32] = 0.0, 1.0          # position 1: pair 0 turned by 90 degrees
+    cs[2, 3], cs[2, 35] = 0.0, -1.0         # position 2: pair 3 turned by -90 degrees
+    cs[2, 5] = -1.0                         # ... and pair 5 by 180 degrees
+    ok = True
+    for neox in (True, False):
+        got = mod.rope_bf16(np.stack([x_bits] * 3)[:, None, :], np.array([0, 1, 2]), cs, neox)[:, 0]
+        ia = lambda i: i if neox else 2 * i  # noqa: E731  first element of pair i
+        ib = lambda i: i + 32 if neox else 2 * i + 1  # noqa: E731
+        want = np.stack([x.copy() for _ in range(3)])
+        want[1, ia(0)], want[1, ib(0)] = -x[ib(0)], x[ia(0)]
+        want[2, ia(3)], want[2, ib(3)] = x[ib(3)], -x[ia(3)]
+        want[2, ia(5)], want[2, ib(5)] = -x[ia(5)], -x[ib(5)]
+        ok &= np.array_equal(O.decode_bf16(got), want) and np.array_equal(got[0], x_bits)
+    return bool(ok)
+
+
+def pin_rope_bf16_against_torch(mod):
+    """rope_bf16 on a RoFormer table against the same rotation done with
+    torch float32 tensor ops (each product and sum its own rounded op) and
+    torch's bf16 cast, for both pairings."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(14)
+    x_bits = W_bits(rng.standard_normal((5, 2, 64)).astype(np.float32))
+    cs = roformer_cache(300).astype(np.float32)
+    pos = np.array([0, 3, 77, 150, 299])
+    ok = True
+    for neox in (True, False):
+        xt = torch.from_numpy(O.decode_bf16(x_bits).astype(np.float32))
+        c = torch.from_numpy(cs[pos, :32])[:, None, :]
+        s_ = torch.from_numpy(cs[pos, 32:])[:, None, :]
+        if neox:
+            a, b = xt[..., :32], xt[..., 32:]
+            r = torch.cat([torch.sub(torch.mul(a, c), torch.mul(b, s_)), torch.add(torch.mul(b, c), torch.mul(a, s_))],
+                          dim=-1)
+        else:
+            a, b = xt[..., 0::2], xt[..., 1::2]
+            r = torch.stack([torch.sub(torch.mul(a, c), torch.mul(b, s_)), torch.add(torch.mul(b, c), torch.mul(a, s_))],
+                            dim=-1).reshape(xt.shape)
+        want = r.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        ok &= np.array_equal(mod.rope_bf16(x_bits, pos, cs, neox), want)
+    return bool(ok)
+
+
+def W_bits(x32):
+    """float32 -> bf16 bits by torch's cast (input generation for the pins)."""
+    torch = pytest.importorskip("torch")
+    return torch.from_numpy(np.ascontiguousarray(x32, dtype=np.float32)).to(torch.bfloat16).view(
+        torch.int16).numpy().view(np.uint16)
+
+
 def all_pins(mod):
     return [pin_hand_rotation(mod), pin_rotation_properties(mod), pin_pairings_differ_by_permutation(mod),
             pin_e4m3_rounding(mod), pin_against_torch(mod), pin_cache_write_round_trip(mod),
-            pin_f32_tracks_f64(mod)]
+            pin_f32_tracks_f64(mod), pin_bf16_rounding(mod), pin_bf16_against_torch(mod),
+            pin_rope_bf16_quarter_turns(mod), pin_rope_bf16_against_torch(mod)]
 
 
 def test_hand_rotation():
@@ -165,6 +266,22 @@ def test_e4m3_against_torch():
 
 def test_cache_write_round_trip():
     assert pin_cache_write_round_trip(K)
+
+
+def test_bf16_rounding():
+    assert pin_bf16_rounding(K)
+
+
+def test_bf16_against_torch():
+    assert pin_bf16_against_torch(K)
+
+
+def test_rope_bf16_quarter_turns():
+    assert pin_rope_bf16_quarter_turns(K)
+
+
+def test_rope_bf16_against_torch():
+    assert pin_rope_bf16_against_torch(K)
 
 
 def test_rope_quantize_shapes_and_values():
@@ -226,6 +343,21 @@ MUTATIONS = [
      "((d_hi == d_lo) & (hi % 2 == 0))", "(d_hi == d_lo)"),
     ("sign dropped",
      "    return (code | (neg.astype(np.uint8) << 7)).astype(np.uint8)", "    return code"),
+    ("bf16 ties away from zero",
+     "    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16", "    u = (u + 0x8000) >> 16"),
+    ("bf16 ties to odd",
+     "    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16", "    u = (u + 0x8000 - ((u >> 16) & 1)) >> 16"),
+    ("bf16 truncation",
+     "    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16", "    u = u >> 16"),
+    ("bf16 wrong shift",
+     "    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16", "    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 15"),
+    ("bf16 parity bit taken from the dropped half",
+     "    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16", "    u = (u + 0x7FFF + ((u >> 15) & 1)) >> 16"),
+    ("bf16 NaN carried into infinity",
+     "    u = np.where(nan, ", "    u = np.where(False, "),
+    ("rope bf16 cos and sin columns swapped",
+     "    cos = cs[(slice(None),) + extra + (slice(0, ROPE_DIM // 2),)]\n    sin = cs[(slice(None),) + extra + (slice(ROPE_DIM // 2, ROPE_DIM),)]",
+     "    sin = cs[(slice(None),) + extra + (slice(0, ROPE_DIM // 2),)]\n    cos = cs[(slice(None),) + extra + (slice(ROPE_DIM // 2, ROPE_DIM),)]"),
     ("slot split by the wrong page size",
      "        kv[slot // page_size, slot % page_size] = rows[t]", "        kv[slot // 64, slot % 64] = rows[t]"),
 ]

@@ -223,3 +223,126 @@ def test_wide_batch_large_schedule():
     db, out, lse = run_gpu(w)
     assert len(db.plan.segments()) > 448
     check(w, out, lse, *oracle(w))
+
+
+# ---------------------------------------------------------------- non-finite and large scores
+
+BF16_NAN = 0x7FC0
+E4M3_NAN = 0x7F
+
+
+def check_nan_rows(w, out, lse, ref_out, ref_lse):
+    """Rows the definition makes NaN are NaN everywhere (out and lse); every
+    other row is checked with the usual tolerances."""
+    got = out.float().cpu().numpy().astype(np.float64)
+    got_lse = lse.cpu().numpy().astype(np.float64)
+    nan_rows = np.isnan(ref_lse)
+    assert nan_rows.any()
+    assert np.all(np.isnan(got_lse[nan_rows])), "a NaN score must make the row's lse NaN"
+    assert np.all(np.isnan(got[nan_rows])), "a NaN score must make the row's output NaN"
+    keep = ~nan_rows.any(axis=1)  # tokens with no NaN row
+    check(w, out, lse, ref_out, ref_lse, rows=keep)
+
+
+@pytest.mark.parametrize("where", ["latent", "rope", "query"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_nan_in_visible_row(where, kv_dtype):
+    """One NaN in a visible cache row (latent or rope column) of a request
+    split over many workers, or in one head's query: the rows that read it
+    are NaN, as the float64 definition gives, on both CTAs of the pair (the
+    24-bit score code keeps NaN a NaN) and through the LSE combine; every
+    other row matches the oracle."""
+    lens = [3000, 9000, 500, 0]
+    w = W.make_workload("dsv3", seed=21, seq_lens=lens, num_heads=128, kv_dtype=kv_dtype,
+                        k_scale=0.5 if kv_dtype == "e4m3" else 1.0)
+    nan = BF16_NAN if kv_dtype == "bf16" else E4M3_NAN
+    key = 7000  # request 1: in a later split of the request
+    page, off = w.block_table[1, key // w.page_size], key % w.page_size
+    if where == "latent":
+        w.kv_bits[page, off, 100] = nan
+    elif where == "rope":
+        w.kv_bits[page, off, 530] = nan
+    else:
+        w.q_nope_bits[2, 17, 5] = BF16_NAN  # request 2, head 17 only
+    db, out, lse = run_gpu(w)
+    assert db.plan.num_partial_slots > 0
+    ref_out, ref_lse = oracle(w)
+    check_nan_rows(w, out, lse, ref_out, ref_lse)
+    if where == "query":
+        assert np.isnan(lse.cpu().numpy()).sum() == 1
+    else:
+        assert np.all(np.isnan(lse.cpu().numpy()[1]))
+
+
+def _scaled_query(w, factor, seed):
+    """Replace the query with bf16 of N(0, factor^2): sharp attention with
+    partial logits in the tens to about a hundred (natural-log units)."""
+    rng = np.random.default_rng(seed)
+    w.q_nope_bits = W.f32_to_bf16_bits(rng.standard_normal(w.q_nope_bits.shape).astype(np.float32) * factor)
+    w.q_pe_bits = W.f32_to_bf16_bits(rng.standard_normal(w.q_pe_bits.shape).astype(np.float32) * factor)
+    return w
+
+
+@pytest.mark.parametrize("factor", [8.0, 16.0])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_large_logits_scaled_query(factor, kv_dtype):
+    """Queries 8x and 16x the benchmark's: logits reach ~100, the lazy
+    rescale fires and the pair's 24-bit partial scores carry large values;
+    requests are split, so the combine merges lse values far apart."""
+    lens = [4096, 20000, 700, 64, 1, 3000, 12000, 2500]
+    w = W.make_workload("dsv3", seed=22, seq_lens=lens, kv_dtype=kv_dtype,
+                        k_scale=0.5 if kv_dtype == "e4m3" else 1.0)
+    _scaled_query(w, factor, seed=23)
+    ref_out, ref_lse = oracle(w)
+    # the case really is sharp: scores far beyond the unit-variance data
+    assert np.nanmax(ref_lse) > 40.0
+    db, out, lse = run_gpu(w)
+    assert db.plan.num_partial_slots > 0
+    check(w, out, lse, ref_out, ref_lse)
+
+
+def _query_direction(w, b):
+    """Unit 576-vector along the sum of request b's query heads (float64): a
+    cache row along it scores high for nearly every head."""
+    t = b * w.q_len
+    u = np.concatenate([O.decode_bf16(w.q_nope_bits[t]).sum(axis=0), O.decode_bf16(w.q_pe_bits[t]).sum(axis=0)])
+    return u / np.linalg.norm(u)
+
+
+def _set_row(w, b, key, values):
+    page, off = w.block_table[b, key // w.page_size], key % w.page_size
+    if w.kv_dtype == "bf16":
+        w.kv_bits[page, off] = W.f32_to_bf16_bits(values.astype(np.float32))
+    else:
+        w.kv_bits[page, off] = W.f32_to_e4m3fn_bits((values / w.k_scale).astype(np.float32))
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_spike_keys_force_rescales(kv_dtype):
+    """Keys whose scores jump far above everything before them, placed in
+    the middle of a segment, on the first key of every split piece, and on a
+    request's last key; plus a request whose whole first tile scores ~40
+    below the rest.  The running maximum then moves by far more than the
+    lazy-rescale threshold (2^8) mid-segment and across split boundaries."""
+    lens = [12000, 6000, 3000, 2100]
+    w = W.make_workload("dsv3", seed=24, seq_lens=lens, kv_dtype=kv_dtype,
+                        k_scale=0.5 if kv_dtype == "e4m3" else 1.0)
+    plan = B.mla_decode_plan(w.seq_lens, w.page_size, w.num_heads, w.q_len)
+    segs = plan.segments()  # (worker, request, tile_begin, tile_end, slot)
+    for b in range(3):
+        d = _query_direction(w, b)
+        starts = sorted({int(s[2]) * 64 for s in segs if s[1] == b and s[2] > 0})
+        assert b > 1 or starts, "the long requests must be split"
+        # alpha / scale sets the typical spike logit (natural-log units)
+        spikes = [(lens[b] // 3, 15.0), (lens[b] // 2 + 5, 30.0), (lens[b] - 1, 45.0)]
+        spikes += [(k, 12.0 + 8.0 * (i % 4)) for i, k in enumerate(starts)]
+        for key, logit in spikes:
+            _set_row(w, b, key, d * (logit / (w.scale * 2.1)))
+    # request 3: its first tile far below everything after it
+    d = _query_direction(w, 3)
+    for key in range(64):
+        _set_row(w, 3, key, -d * (40.0 / (w.scale * 2.1)))
+    ref_out, ref_lse = oracle(w)
+    assert 40.0 < np.nanmax(ref_lse) < 130.0  # sharp, within the exchange's precision range
+    db, out, lse = run_gpu(w)
+    check(w, out, lse, ref_out, ref_lse)
