@@ -571,16 +571,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& rlo, fl
 
 // ------------------------------------------------------------------ exchange
 
-// Partial scores cross to the peer as 24-bit codes: the float's top 24 bits,
-// rounded to nearest on the 8 dropped mantissa bits (relative error 2^-16).
-// Infinities and NaN (exponent all ones) are truncated instead, with the
-// lowest code bit set for a NaN whose payload sits in the dropped bits:
-// rounding could carry a NaN's mantissa into the sign bit, truncation alone
-// could turn such a NaN into an infinity, and the peer must see the same
-// non-finite score as this CTA.  Four codes fill three words.
+// Partial scores cross to the peer as 24-bit codes: the float's top 24 bits
+// (sign, exponent, 15 mantissa bits).  Rounding is one multiply and a
+// truncation: x * (1 + 85 * 2^-23) adds between 0.332 and 0.664 of a code unit
+// to |x| (in proportion to the mantissa), so the dropped bits round the kept
+// ones with an error of at most 0.668 of a code unit, a relative error below
+// (4/3) * 2^-16.  Because it is a floating-point multiply, every NaN becomes
+// the canonical NaN (top bits all ones, still a NaN after the truncation) and
+// infinities stay infinite, so both CTAs of the pair see the same non-finite
+// score; an integer rounding add would carry the canonical NaN's mantissa into
+// the sign bit.  Four codes fill three words.
+constexpr float kCodeRound = 1.00001013278961181640625f;  // 1 + 85 * 2^-23, exact in float32
 __device__ __forceinline__ uint32_t score24(uint32_t bits) {
-  if ((bits & 0x7F800000u) == 0x7F800000u) return (bits >> 8) | ((bits & 0x007FFFFFu) != 0u ? 1u : 0u);
-  return (bits + 0x80u) >> 8;
+  return __float_as_uint(__uint_as_float(bits) * kCodeRound) >> 8;
 }
 __device__ __forceinline__ void pack24(const uint32_t* v, uint32_t* w) {
   const uint32_t a = score24(v[0]), b = score24(v[1]), c = score24(v[2]), d = score24(v[3]);

@@ -227,10 +227,6 @@ def test_wide_batch_large_schedule():
 
 # ---------------------------------------------------------------- non-finite and large scores
 
-BF16_NAN = 0x7FC0
-E4M3_NAN = 0x7F
-
-
 def check_nan_rows(w, out, lse, ref_out, ref_lse):
     """Rows the definition makes NaN are NaN everywhere (out and lse); every
     other row is checked with the usual tolerances."""
@@ -244,18 +240,25 @@ def check_nan_rows(w, out, lse, ref_out, ref_lse):
     check(w, out, lse, ref_out, ref_lse, rows=keep)
 
 
+# NaN bit patterns: quiet, negative quiet, and a payload in the lowest bit
+BF16_NANS = {"qnan": 0x7FC0, "neg_qnan": 0xFFC0, "low_payload": 0x7F81}
+E4M3_NANS = {"qnan": 0x7F, "neg_qnan": 0xFF, "low_payload": 0x7F}  # e4m3fn has one NaN code per sign
+
+
+@pytest.mark.parametrize("pattern", list(BF16_NANS))
 @pytest.mark.parametrize("where", ["latent", "rope", "query"])
 @pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
-def test_nan_in_visible_row(where, kv_dtype):
+def test_nan_in_visible_row(pattern, where, kv_dtype):
     """One NaN in a visible cache row (latent or rope column) of a request
     split over many workers, or in one head's query: the rows that read it
     are NaN, as the float64 definition gives, on both CTAs of the pair (the
-    24-bit score code keeps NaN a NaN) and through the LSE combine; every
-    other row matches the oracle."""
+    24-bit score code keeps the tensor core's NaN results NaN) and through the
+    LSE combine; every other row matches the oracle.  NaN of either sign and
+    with its payload in the lowest bit all behave the same."""
     lens = [3000, 9000, 500, 0]
     w = W.make_workload("dsv3", seed=21, seq_lens=lens, num_heads=128, kv_dtype=kv_dtype,
                         k_scale=0.5 if kv_dtype == "e4m3" else 1.0)
-    nan = BF16_NAN if kv_dtype == "bf16" else E4M3_NAN
+    nan = BF16_NANS[pattern] if kv_dtype == "bf16" else E4M3_NANS[pattern]
     key = 7000  # request 1: in a later split of the request
     page, off = w.block_table[1, key // w.page_size], key % w.page_size
     if where == "latent":
@@ -263,7 +266,7 @@ def test_nan_in_visible_row(where, kv_dtype):
     elif where == "rope":
         w.kv_bits[page, off, 530] = nan
     else:
-        w.q_nope_bits[2, 17, 5] = BF16_NAN  # request 2, head 17 only
+        w.q_nope_bits[2, 17, 5] = BF16_NANS[pattern]  # request 2, head 17 only
     db, out, lse = run_gpu(w)
     assert db.plan.num_partial_slots > 0
     ref_out, ref_lse = oracle(w)
