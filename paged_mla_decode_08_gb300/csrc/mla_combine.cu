@@ -14,9 +14,11 @@
 // of 8 output columns), so that the producing kernel stores coalesced.  One
 // CTA of 256 threads per (job, block of 32 query rows, quarter of the 64
 // chunks): a warp owns 2 chunks and reads them for 32 consecutive rows (512
-// contiguous bytes per chunk and split); the partials of the first four
-// splits are requested before the split weights e^{lse_s - lse} are computed
-// (one warp, into shared memory), so both memory latencies overlap; the
+// contiguous bytes per chunk and split); the partials of the first 4, 8 or 16
+// splits (a group sized for the widest job of the launch) are requested
+// before the split weights e^{lse_s - lse} are computed (one warp, into
+// shared memory), so both memory latencies overlap, and later groups are
+// loaded one round each; the
 // 32 x 128 bf16 result is transposed through shared memory so that each
 // output row segment is written with contiguous 16-byte stores.  The bf16
 // partials add one rounding of O_s (relative 2^-9) before the merge, well
@@ -44,12 +46,15 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 }
 
 // One (job, 32-row block, quarter of the columns) of the merge; called after
-// the grid dependency wait.
-__device__ __forceinline__ void combine_body(const CombineJob job, const DecodeArgs& a) {
+// the grid dependency wait.  kGroup splits' partials are in flight at a time:
+// the merge is a chain of dependent load rounds (ceil(nsplit / kGroup) of
+// them), so requests split many ways take a wider group.
+template <int kGroup>
+__device__ __forceinline__ void combine_body(const CombineJob job, const DecodeArgs& a, int row_block, int quarter) {
   extern __shared__ float s_w[];  // [nsplit][32] weights (0 for -inf splits)
   const int M = a.rows;  // partial-row stride: the planned rows per request
-  const int r0 = blockIdx.y * kCombRows;
-  const int c0 = blockIdx.z * kCombChunks;
+  const int r0 = row_block * kCombRows;
+  const int c0 = quarter * kCombChunks;
   // this request's query rows (fewer than M in a ragged batch) and where
   // they go in out / lse
   const int2 q = request_q(a, job.req);
@@ -65,7 +70,6 @@ __device__ __forceinline__ void combine_body(const CombineJob job, const DecodeA
   // The partials of the first kGroup splits do not depend on the weights:
   // their loads go out before the lse values are even read, so the two
   // memory round trips overlap.
-  constexpr int kGroup = 4;
   uint4 v[kGroup][2];
 #pragma unroll
   for (int g = 0; g < kGroup; ++g)
@@ -150,23 +154,24 @@ __device__ __forceinline__ void combine_body(const CombineJob job, const DecodeA
 // overlaps the main kernel's tail; the partials are read after the wait
 // (which returns once the main grid has completed and its writes are
 // visible; without the launch attribute it returns at once).
-template <int CAP>
+template <int CAP, int kGroup>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineList<CAP> jobs,
                                                       const __grid_constant__ DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  combine_body(jobs.job[blockIdx.x], a);
+  combine_body<kGroup>(jobs.job[blockIdx.x], a, blockIdx.y, blockIdx.z);
 }
 
 // Device plan: the job list is in the workspace, written by the planner
 // grid two launches earlier (read at L2, ld.global.cg, like the schedule);
-// the grid covers the most jobs any plan can have and CTAs past the actual
-// count return.
+// the grid covers the most jobs any plan for the batch can have and CTAs past
+// the actual count return.
 __global__ void __launch_bounds__(256) combine_kernel_dev(const CombineList<kJobCap>* jobs,
                                                           const __grid_constant__ DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if ((int)blockIdx.x >= __ldcg(&jobs->num_jobs)) return;
   const CombineJob* j = &jobs->job[blockIdx.x];  // 4-byte loads: no alignment assumed
-  combine_body(CombineJob{__ldcg(&j->req), __ldcg(&j->slot_begin), __ldcg(&j->nsplit), 0}, a);
+  combine_body<4>(CombineJob{__ldcg(&j->req), __ldcg(&j->slot_begin), __ldcg(&j->nsplit), 0}, a, blockIdx.y,
+                  blockIdx.z);
 }
 
 template <int CAP>
@@ -191,7 +196,10 @@ static cudaError_t launch_combine_cap(const std::vector<CombineJob>& jobs, const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel<CAP>, list, a);
+  // splits in flight per load round: enough for the widest job, within reason
+  if (maxsplit <= 4) return cudaLaunchKernelEx(&cfg, combine_kernel<CAP, 4>, list, a);
+  if (maxsplit <= 8) return cudaLaunchKernelEx(&cfg, combine_kernel<CAP, 8>, list, a);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<CAP, 16>, list, a);
 }
 
 cudaError_t launch_combine(const std::vector<CombineJob>& jobs, const DecodeArgs& a,
@@ -205,7 +213,10 @@ cudaError_t launch_combine_dev(int workers, const DecodeArgs& a, const void* wor
   const auto* jobs = reinterpret_cast<const CombineList<kJobCap>*>(static_cast<const char*>(workspace) +
                                                                     kDevJobsOffset);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(workers - 1), (unsigned)((a.rows + kCombRows - 1) / kCombRows),
+  // at most one job per split request: fewer than the workers, and no more
+  // than the requests
+  const int max_jobs = workers - 1 < a.batch ? workers - 1 : a.batch;
+  cfg.gridDim = dim3((unsigned)max_jobs, (unsigned)((a.rows + kCombRows - 1) / kCombRows),
                      (unsigned)(kChunks / kCombChunks));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = (size_t)workers * kCombRows * sizeof(float);  // a request spans <= W workers

@@ -21,11 +21,16 @@
 // boundary there are at most W - 1 jobs and 2 (W - 1) slots, and at most
 // batch + W - 1 segments.
 //
-// One CTA of 1024 threads: a request is handled by one thread (two when the
-// batch exceeds 1024), prefix sums are block scans, and worker_seg is a
-// lower bound of each worker in the sorted segment-worker array.  The grid is
-// launched ahead of the decode on the same stream and lets the decode's
-// prologue start early (programmatic dependent launch).
+// One CTA of as many warps as the batch needs (two requests per thread, up
+// to 1024 threads): a single warp for up to 64 requests, whose scans then
+// need no block barrier work.  Prefix sums are block scans (one for the
+// costs, one for the segment, slot and job counts packed into one 64-bit
+// word), and worker_seg is a lower bound of each worker in the sorted
+// segment-worker array.  The grid is launched ahead of the decode on the same
+// stream and lets the decode's prologue start early (programmatic dependent
+// launch).  (Running this rule inside the decode's own prologue instead, in
+// every CTA, was measured slower: its cold length load and scans then sit on
+// every CTA's path, where here they overlap the decode's launch.)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,7 +45,7 @@ constexpr int kPerThread = 2;
 // Exclusive prefix sum over the block of one 64-bit value per thread; every
 // thread also receives the total.
 __device__ long long block_exclusive_scan(long long v, long long* total, long long* s_warp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   long long x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -50,7 +55,7 @@ __device__ long long block_exclusive_scan(long long v, long long* total, long lo
   if (lane == 31) s_warp[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    long long w = s_warp[lane];
+    long long w = lane < nwarps ? s_warp[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const long long y = __shfl_up_sync(0xffffffffu, w, o);
@@ -60,7 +65,7 @@ __device__ long long block_exclusive_scan(long long v, long long* total, long lo
   }
   __syncthreads();
   const long long before = (warp > 0 ? s_warp[warp - 1] : 0) + x - v;
-  *total = s_warp[31];
+  *total = s_warp[nwarps - 1];
   __syncthreads();  // s_warp is reused by the next scan
   return before;
 }
@@ -94,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int k = 0; k < kPerThread; ++k) {
     const int b = threadIdx.x * kPerThread + k;
-    int L = b < batch ? seq_lens[b] : 0;
+    int L = b < batch ? __ldg(seq_lens + b) : 0;
     L = L < 0 ? 0 : (L < cap_tokens ? L : cap_tokens);  // the decode's clamp
     n[k] = (L + kTileTokens - 1) / kTileTokens;
     cost += b < batch ? n[k] + kSegOverheadTiles : 0;
@@ -129,10 +134,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       pc[k] = Piece{0, 0};
     }
   }
-  long long nseg_total, slots_total, jobs_total;
-  int seg_base = (int)block_exclusive_scan(nseg_t, &nseg_total, s_warp);
-  int slot_base = (int)block_exclusive_scan(slots_t, &slots_total, s_warp);
-  int job_base = (int)block_exclusive_scan(jobs_t, &jobs_total, s_warp);
+  // one scan for the three counts, 21 bits each (each total is at most
+  // batch + workers - 1 < 2^21)
+  long long packed_total;
+  const long long packed = block_exclusive_scan((long long)nseg_t | ((long long)slots_t << 21) | ((long long)jobs_t << 42),
+                                                &packed_total, s_warp);
+  const long long m21 = (1LL << 21) - 1;
+  int seg_base = (int)(packed & m21);
+  int slot_base = (int)((packed >> 21) & m21);
+  int job_base = (int)(packed >> 42);
+  const long long nseg_total = packed_total & m21, jobs_total = packed_total >> 42;
 
   // ---- segments and combine jobs
 #pragma unroll
@@ -165,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- worker_seg[w] = first segment whose worker is >= w
   const int total_segs = (int)nseg_total;
-  for (int w = threadIdx.x; w <= workers; w += kThreads) {
+  for (int w = threadIdx.x; w <= workers; w += blockDim.x) {
     int lo = 0, hi = total_segs;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
@@ -187,7 +198,10 @@ cudaError_t launch_plan_device(const int32_t* seq_lens, int batch, int cap_token
                                cudaStream_t stream) {
   auto* sched = reinterpret_cast<Schedule<kSegCapLarge>*>(static_cast<char*>(workspace) + kDevSchedOffset);
   auto* jobs = reinterpret_cast<CombineList<kJobCap>*>(static_cast<char*>(workspace) + kDevJobsOffset);
-  devplan::plan_kernel<<<1, devplan::kThreads, 0, stream>>>(seq_lens, batch, cap_tokens, workers, sched, jobs);
+  // two requests per thread, whole warps, at most kThreads
+  int threads = ((batch + devplan::kPerThread - 1) / devplan::kPerThread + 31) / 32 * 32;
+  threads = threads < 32 ? 32 : (threads > devplan::kThreads ? devplan::kThreads : threads);
+  devplan::plan_kernel<<<1, threads, 0, stream>>>(seq_lens, batch, cap_tokens, workers, sched, jobs);
   return cudaGetLastError();
 }
 

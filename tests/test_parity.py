@@ -349,3 +349,19 @@ def test_spike_keys_force_rescales(kv_dtype):
     assert 40.0 < np.nanmax(ref_lse) < 130.0  # sharp, within the exchange's precision range
     db, out, lse = run_gpu(w)
     check(w, out, lse, ref_out, ref_lse)
+
+
+@pytest.mark.parametrize("lens,widest", [
+    ([4096] * 24, (2, 4)),      # splits of at most 4: four partials per load round
+    ([4096] * 10, (5, 8)),      # 5-8: eight per round
+    ([60000, 500, 33], (9, 128)),  # many: sixteen per round
+])
+def test_combine_group_sizes(lens, widest):
+    """The combine loads the partials of 4, 8 or 16 splits per round, chosen
+    for the widest split of the launch; each width merges like the oracle."""
+    w = W.make_workload("dsv3", seed=25, seq_lens=lens)
+    db, out, lse = run_gpu(w)
+    segs = db.plan.segments()
+    most = max(int((segs[:, 1] == b).sum()) for b in range(len(lens)))
+    assert widest[0] <= most <= widest[1], most
+    check(w, out, lse, *oracle(w))
