@@ -7,9 +7,9 @@
 //
 // Work item = 8 elements of one row: a chunk of the 512 latent columns, or 4
 // rotated pairs of the 64 rope columns; a token has (num_heads + 1) rows of
-// 72 items (its query heads, then its key).  One thread per item, flat grid:
-// the loads are 16-byte (8-byte for a half-split rope chunk), the stores
-// 8 or 16 bytes.  Memory bound: per token 1152 B read per head and per key,
+// 72 items (its query heads, then its key).  One thread per item: the loads
+// are 16-byte (8-byte for a half-split rope chunk), the stores 8 or 16
+// bytes.  Memory bound: per token 1152 B read per head and per key,
 // 576 (e4m3) or 1152 (bf16) bytes written per output row.
 //
 // Rotation: pair (a, b) -> (a cos - b sin, b cos + a sin) in fp32 (each
@@ -62,17 +62,26 @@ struct Args {
   int num_tokens, num_heads, q_e4m3, kv_e4m3, is_neox;
 };
 
-// Load 4 rope pairs (4r .. 4r + 3) of a 64-wide bf16 row as floats.
-__device__ __forceinline__ void load_pairs(const uint16_t* row, int r, bool neox, float a[4], float b[4]) {
+// The raw bits of 4 rope pairs (4r .. 4r + 3) of a 64-wide bf16 row: for
+// is_neox the 8 bytes of elements 4r.. and the 8 bytes of elements 32 + 4r..,
+// otherwise the 16 bytes of elements 8r..
+__device__ __forceinline__ uint4 load_pairs_raw(const uint16_t* row, int r, bool neox) {
   if (neox) {
     const uint2 x = *reinterpret_cast<const uint2*>(row + 4 * r);
     const uint2 y = *reinterpret_cast<const uint2*>(row + 32 + 4 * r);
-    a[0] = bf_lo(x.x); a[1] = bf_hi(x.x); a[2] = bf_lo(x.y); a[3] = bf_hi(x.y);
-    b[0] = bf_lo(y.x); b[1] = bf_hi(y.x); b[2] = bf_lo(y.y); b[3] = bf_hi(y.y);
+    return make_uint4(x.x, x.y, y.x, y.y);
+  }
+  return *reinterpret_cast<const uint4*>(row + 8 * r);
+}
+
+// ... and as floats: a[k], b[k] are the two elements of pair 4r + k.
+__device__ __forceinline__ void unpack_pairs(uint4 v, bool neox, float a[4], float b[4]) {
+  if (neox) {
+    a[0] = bf_lo(v.x); a[1] = bf_hi(v.x); a[2] = bf_lo(v.y); a[3] = bf_hi(v.y);
+    b[0] = bf_lo(v.z); b[1] = bf_hi(v.z); b[2] = bf_lo(v.w); b[3] = bf_hi(v.w);
   } else {
-    const uint4 x = *reinterpret_cast<const uint4*>(row + 8 * r);
-    a[0] = bf_lo(x.x); b[0] = bf_hi(x.x); a[1] = bf_lo(x.y); b[1] = bf_hi(x.y);
-    a[2] = bf_lo(x.z); b[2] = bf_hi(x.z); a[3] = bf_lo(x.w); b[3] = bf_hi(x.w);
+    a[0] = bf_lo(v.x); b[0] = bf_hi(v.x); a[1] = bf_lo(v.y); b[1] = bf_hi(v.y);
+    a[2] = bf_lo(v.z); b[2] = bf_hi(v.z); a[3] = bf_lo(v.w); b[3] = bf_hi(v.w);
   }
 }
 
@@ -123,62 +132,66 @@ __device__ __forceinline__ void rotate4(const float x[4], const float y[4], cons
   }
 }
 
+// One thread per item over a flat grid.  Each thread issues its independent
+// loads -- the position, the slot and the source chunk -- before anything
+// that depends on them, then the cos / sin pair the position selects: two
+// memory round trips in all.
 __global__ void __launch_bounds__(kThreads) rope_quantize_write_kernel(const Args a) {
   const int64_t item = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-  const int64_t per_token = (int64_t)(a.num_heads + 1) * kItemsPerRow;
-  if (item >= per_token * a.num_tokens) return;
+  const int per_token = (a.num_heads + 1) * kItemsPerRow;
+  if (item >= (int64_t)per_token * a.num_tokens) return;
   const int t = (int)(item / per_token);
   const int rem = (int)(item - (int64_t)t * per_token);
   const int h = rem / kItemsPerRow;  // h == num_heads: the key row
   const int w = rem - h * kItemsPerRow;
   const bool is_key = h == a.num_heads;
-
-  // rotation of this token (identity without a cos/sin table)
-  float c[4] = {1.f, 1.f, 1.f, 1.f}, sn[4] = {0.f, 0.f, 0.f, 0.f};
-  if (w >= 64 && a.cos_sin) {
-    const int64_t pos = a.positions[t];
-    if (pos < 0 || pos >= a.max_position) {
-      if (w == 64 && (is_key || h == 0)) record(0x601);
-      return;  // nothing of this token is written
-    }
-    const int r = w - 64;
-    const float4 cv = *reinterpret_cast<const float4*>(a.cos_sin + pos * 64 + 4 * r);
-    const float4 sv = *reinterpret_cast<const float4*>(a.cos_sin + pos * 64 + 32 + 4 * r);
-    c[0] = cv.x; c[1] = cv.y; c[2] = cv.z; c[3] = cv.w;
-    sn[0] = sv.x; sn[1] = sv.y; sn[2] = sv.z; sn[3] = sv.w;
-  } else if (a.cos_sin) {
-    const int64_t pos = a.positions[t];
-    if (pos < 0 || pos >= a.max_position) return;  // recorded by the rope items
+  // ---- independent loads
+  const int64_t pos = a.cos_sin ? a.positions[t] : 0;
+  const int64_t slot = is_key ? a.slots[t] : 0;
+  const int64_t qrow = (int64_t)t * a.num_heads + h;
+  uint4 x = make_uint4(0u, 0u, 0u, 0u);
+  if (w < 64) {
+    if (is_key)
+      x = *reinterpret_cast<const uint4*>(a.k_nope + (int64_t)t * 512 + 8 * w);
+    else if (a.q_e4m3)
+      x = *reinterpret_cast<const uint4*>(a.q_nope + qrow * 512 + 8 * w);
+  } else {
+    x = load_pairs_raw(is_key ? a.k_rope + (int64_t)t * 64 : a.q_rope + qrow * 64, w - 64, a.is_neox);
   }
-
+  if (a.cos_sin && (pos < 0 || pos >= a.max_position)) {
+    if (w == 64 && (is_key || h == 0)) record(0x601);
+    return;  // nothing of this token is written
+  }
+  // ---- rotation of the rope chunks (identity without a cos/sin table)
+  float ra[4], rb[4];
+  if (w >= 64) {
+    float c[4] = {1.f, 1.f, 1.f, 1.f}, sn[4] = {0.f, 0.f, 0.f, 0.f};
+    if (a.cos_sin) {
+      const int r = w - 64;
+      const float4 cv = *reinterpret_cast<const float4*>(a.cos_sin + pos * 64 + 4 * r);
+      const float4 sv = *reinterpret_cast<const float4*>(a.cos_sin + pos * 64 + 32 + 4 * r);
+      c[0] = cv.x; c[1] = cv.y; c[2] = cv.z; c[3] = cv.w;
+      sn[0] = sv.x; sn[1] = sv.y; sn[2] = sv.z; sn[3] = sv.w;
+    }
+    float xa[4], xb[4];
+    unpack_pairs(x, a.is_neox, xa, xb);
+    rotate4(xa, xb, c, sn, ra, rb);
+  }
+  // ---- stores
   if (is_key) {
-    const int64_t slot = a.slots[t];
     if (slot < 0 || slot >= a.num_slots) {
       if (w == 0) record(0x602);
       return;
     }
-    void* row = static_cast<uint8_t*>(a.kv) + slot * (a.kv_e4m3 ? 576 : 1152);
-    if (w < 64) {
-      const uint4 x = *reinterpret_cast<const uint4*>(a.k_nope + (int64_t)t * 512 + 8 * w);
-      store_latent(static_cast<uint8_t*>(row) + (a.kv_e4m3 ? 8 : 16) * w, a.kv_e4m3, x);
-    } else {
-      float x[4], y[4], ra[4], rb[4];
-      load_pairs(a.k_rope + (int64_t)t * 64, w - 64, a.is_neox, x, y);
-      rotate4(x, y, c, sn, ra, rb);
-      store_pairs(static_cast<uint8_t*>(row) + (a.kv_e4m3 ? 512 : 1024), a.kv_e4m3, w - 64, a.is_neox, ra, rb);
-    }
-    return;
-  }
-
-  const int64_t qrow = (int64_t)t * a.num_heads + h;
-  if (w < 64) {
-    if (!a.q_e4m3) return;  // bf16 query: the latent part is used as it is
-    const uint4 x = *reinterpret_cast<const uint4*>(a.q_nope + qrow * 512 + 8 * w);
-    store_latent(static_cast<uint8_t*>(a.q_out) + qrow * 576 + 8 * w, true, x);
+    uint8_t* row = static_cast<uint8_t*>(a.kv) + slot * (a.kv_e4m3 ? 576 : 1152);
+    if (w < 64)
+      store_latent(row + (a.kv_e4m3 ? 8 : 16) * w, a.kv_e4m3, x);
+    else
+      store_pairs(row + (a.kv_e4m3 ? 512 : 1024), a.kv_e4m3, w - 64, a.is_neox, ra, rb);
+  } else if (w < 64) {
+    if (a.q_e4m3)  // a bf16 query's latent part is used as it is
+      store_latent(static_cast<uint8_t*>(a.q_out) + qrow * 576 + 8 * w, true, x);
   } else {
-    float x[4], y[4], ra[4], rb[4];
-    load_pairs(a.q_rope + qrow * 64, w - 64, a.is_neox, x, y);
-    rotate4(x, y, c, sn, ra, rb);
     void* dst = a.q_e4m3 ? static_cast<void*>(static_cast<uint8_t*>(a.q_out) + qrow * 576 + 512)
                          : static_cast<void*>(static_cast<uint16_t*>(a.q_out) + qrow * 64);
     store_pairs(dst, a.q_e4m3, w - 64, a.is_neox, ra, rb);

@@ -107,6 +107,28 @@ def test_plain_cache_write_without_rotation_or_query():
     assert np.array_equal(kv.cpu().numpy().view(np.uint16), K.kv_cache_write(st["kv"], rows, st["slots"], 64))
 
 
+def test_more_tokens_than_one_grid_column():
+    """70,000 new tokens: the launch covers at most 65,535 tokens per grid
+    column and loops over the rest.  Every cache row must be rewritten, and a
+    sample of tokens on both sides of the 65,535 boundary must match the
+    oracle bit for bit (query codes and cache rows)."""
+    t = 70_000
+    st = make_step(8, t, 1, 64, "e4m3", pool_pages=t // 64 + 8)
+    q_out, kv, err = run_kernel(st, B.MLA_Q_E4M3, "e4m3", False)
+    assert err == 0
+    sample = np.unique(np.concatenate([np.arange(0, 64), np.arange(65_500, 65_600), np.arange(t - 64, t),
+                                       np.random.default_rng(9).integers(0, t, 200)]))
+    qc, kc, _, _ = K.rope_quantize_fp8(st["q_nope"][sample], st["q_rope"][sample], st["k_nope"][sample],
+                                       st["k_rope"][sample], st["pos"][sample], st["cs"], False)
+    assert np.array_equal(q_out[sample], qc)
+    flat_new, flat_old = kv.reshape(-1, 576), st["kv"].reshape(-1, 576)
+    assert np.array_equal(flat_new[st["slots"][sample]], kc)
+    # rows of every token changed (a random 576-byte row rewritten with the same bytes is not a real risk)
+    assert np.all(np.any(flat_new[st["slots"]] != flat_old[st["slots"]], axis=1))
+    untouched = np.setdiff1d(np.arange(flat_old.shape[0]), st["slots"])
+    assert np.array_equal(flat_new[untouched], flat_old[untouched])
+
+
 def test_bad_positions_and_slots_are_reported_not_written():
     st = make_step(6, 4, 2, 64, "e4m3", pool_pages=8, max_pos=100)
     st["pos"][1] = 100      # past the table: token 1 untouched
