@@ -330,6 +330,16 @@ __device__ void producer(const Ctx& c, const S& sched, const DecodeArgs& a, cons
         __syncwarp();
         continue;
       }
+      // The first fill of the ring goes out one tile at a time, each tile
+      // once the previous one has landed.  At kernel start every CTA's copies
+      // compete for HBM; a first tile that travels alone starts the score /
+      // softmax chain microseconds earlier than one that shares the wire
+      // with the whole fill, and the later tiles arrive while the chain
+      // works on it.
+      if (j >= 1 && j < kStages && !wait_bar_warp<false>(c, c.bar(B_KV_FULL + (j - 1)), 0, 0x104)) {
+        ok = false;
+        break;
+      }
       if (j >= kStages && !wait_bar_warp<false>(c, c.bar(B_KV_EMPTY + stage), ((j / kStages) - 1) & 1, 0x101)) {
         ok = false;
         break;
