@@ -10,7 +10,7 @@
 namespace mla {
 
 constexpr int kTileTokens = 64;      // KV tokens per main-loop tile
-constexpr int kSegOverheadTiles = 2; // planner: per-segment cost, in tiles
+constexpr int kSegOverheadTiles = 3; // planner: per-segment cost, in tiles (measured: about 2.6)
 constexpr int kMinSplitTiles = 4;    // planner: shortest piece of a split request
 constexpr int kMaxWorkers = 128;     // persistent CTA pairs (<= 256 SMs)
 constexpr int kMaxRows = 128;        // num_heads * q_len handled by one CTA

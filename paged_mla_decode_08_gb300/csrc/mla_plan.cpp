@@ -8,7 +8,8 @@
 // Rule.  Cut every request into 64-token tiles, n_b = ceil(L_b / 64).  There
 // are W workers (one per CTA pair, W = num_sms / 2, at most 128).  Each
 // segment (a run of tiles of one request on one worker) costs its tiles plus
-// OVH = 2 tiles of fixed work (query load, epilogue).  For a capacity C,
+// OVH = 3 tiles of fixed work (query load, epilogue, pipeline refill: a
+// clock64 trace of the kernel puts it at about 2.6 tiles).  For a capacity C,
 // fill(C) walks the requests in order and pours them into workers 0, 1, ...:
 // a request that fits the worker's room (C - cost so far - OVH) goes there
 // whole; otherwise, when room >= MIN (= 4) and at least 2 MIN tiles are left,

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported():
 
 def test_version_and_constants():
     assert B.mla_decode_version() >= 100
-    assert B.mla_planner_constants() == (64, 2, 4)
+    assert B.mla_planner_constants() == (64, 3, 4)
     assert B.load().mla_decode_last_error_string() is not None
 
 

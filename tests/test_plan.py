@@ -112,7 +112,7 @@ CASES = [(n, s) for n in W.CONFIGS for s in (148, 152)] + [("dsv3", 2), ("fp8_kv
 @pytest.mark.parametrize("name,sms", CASES)
 def test_plan_matches_rule(name, sms):
     tile, ovh, mn = B.mla_planner_constants()
-    assert (tile, ovh, mn) == (64, 2, 4)
+    assert (tile, ovh, mn) == (64, 3, 4)
     cfg = W.CONFIGS[name]
     lens = lens_of(name)
     p = B.mla_decode_plan(lens, cfg["page_size"], cfg["num_heads"], cfg["q_len"], num_sms=sms)

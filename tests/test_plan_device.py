@@ -10,7 +10,7 @@ from paged_mla_decode_08_gb300 import binding as B
 
 from test_plan import check_invariants
 
-TILE, OVH, MIN = 64, 2, 4
+TILE, OVH, MIN = 64, 3, 4  # the library's planner constants (checked in test_abi_host)
 
 
 def device_plan_rule(lens, workers, cap_tokens=1 << 30):
@@ -42,6 +42,10 @@ def device_plan_rule(lens, workers, cap_tokens=1 << 30):
                 slot += ns
         p += nb + OVH
     return np.array(segs, dtype=np.int32).reshape(-1, 5), slot, jobs
+
+
+def test_rule_constants_are_the_librarys():
+    assert B.mla_planner_constants() == (TILE, OVH, MIN)
 
 
 def random_lens(rng, kind, bsz):
