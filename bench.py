@@ -316,8 +316,13 @@ def our_arm(args, w, rank, world):
     value, tot_s = whole_job_rate(sum(step_ms) / 1e3, st["tokens"], K, world, dist, dev)
     ms_per_step = tot_s * 1e3 / K
 
-    # ---- e2e: host buffers in, results back to the host, copies timed
-    e2e = e2e_measure(db, w, dev, stream, max(3, min(K, 200)))
+    # ---- the same host-planned step captured in a CUDA graph and replayed
+    # (no per-launch host work; the lengths are fixed by the plan)
+    graph_s = graph_step_seconds(lambda cs: R.decode(db, cs), dev, stream, flush, max(3, min(K, 200)))
+    # ---- e2e: host buffers in, results back to the host, copies timed;
+    # host-synchronous per step, and with the host link overlapped
+    e2e_serial = e2e_measure(db, w, dev, stream, max(3, min(K, 200)))
+    e2e = e2e_pipelined_measure(db, w, dev, stream, max(3, min(K, 200)))
     # ---- the step before the decode: block-table construction, timed alone
     bt_rows = block_table_measure(w, dev, stream, flush, max(3, min(K, 200)))
     # ---- ragged query counts (draft extend), the same decode kernels
@@ -362,6 +367,7 @@ def our_arm(args, w, rank, world):
                          "sample": f"whole-request float64 oracle passes over the same workload, "
                                    f"{cpu_rows} query tokens in {cpu_el:.1f} s"},
         "e2e": e2e,
+        "e2e_serial": e2e_serial,
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
         "kv_gbs": st["kv_bytes"] / step_avg_s / 1e9,
@@ -374,6 +380,9 @@ def our_arm(args, w, rank, world):
         "wall_s_timed_loop": wall,
         "block_table_build": bt_rows,
         "ragged_decode": ragged,
+        "graph_replay": {"us_per_step": graph_s * 1e6, "tokens_per_s": st["tokens"] / graph_s,
+                         "note": "the same decode step captured once in a CUDA graph and replayed; "
+                                 "L2 flushed between replays"},
         "device_plan": devplan,
         "rope_quantize_write": rope_write,
         "segments": int(len(db.plan.segments())), "partial_slots": db.plan.num_partial_slots,
@@ -544,6 +553,31 @@ def block_table_measure(w, dev, stream, flush, K):
     return res
 
 
+def graph_step_seconds(launch, dev, stream, flush, K):
+    """Capture `launch(capture_stream)` once in a CUDA graph, then time K
+    replays on `stream` (L2 flushed before each, outside the events).
+    Returns the mean seconds per replay."""
+    import torch
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            launch(cap)
+    stream.wait_stream(cap)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for k in range(K):
+            flush.zero_()
+            ev[k][0].record(stream)
+            graph.replay()
+            ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+
+
 def device_plan_measure(db, w, dev, stream, flush, K, st):
     """The headline decode with a device plan: each step launches the planner
     kernel, the main kernel and the combine (what a CUDA graph captured once
@@ -583,13 +617,20 @@ def device_plan_measure(db, w, dev, stream, flush, K, st):
     torch.cuda.synchronize()
     main_us = statistics.mean(e[0].elapsed_time(e[1]) for e in evk) * 1e3
     comb_us = statistics.mean(e[1].elapsed_time(e[2]) for e in evk) * 1e3
+    # the same step captured once in a CUDA graph and replayed (the use the
+    # device plan exists for: no host work and one graph launch per step)
+    g_avg = graph_step_seconds(
+        lambda cs: B.mla_decode(plan, db.q_nope, db.q_pe, db.kv, db.kv_dtype, db.block_table, db.seq_lens,
+                                w.scale, w.k_scale, out, lse, ws, None, cs), dev, stream, flush, K)
     host_out = R.decode(db, stream)[0]
     diff = float((out.float() - host_out.float()).abs().max())  # the two plans split differently
     return {"us_per_step": s_avg * 1e6, "tokens_per_s": st["tokens"] / s_avg,
+            "graph_us_per_step": g_avg * 1e6, "graph_tokens_per_s": st["tokens"] / g_avg,
             "planner_plus_main_us": main_us, "combine_us": comb_us,
             "segments": int(len(plan.device_segments(ws))), "launches_per_step": 3,
             "max_abs_diff_vs_host_plan": diff,
-            "note": "planner + main + combine per step, L2 flushed between steps"}
+            "note": "planner + main + combine per step (eager launches; graph_*: one captured CUDA graph "
+                    "replayed per step), L2 flushed between steps"}
 
 
 def rope_write_measure(w, dev, stream, flush, K, peaks):
@@ -695,6 +736,85 @@ def e2e_measure(db, w, dev, stream, K):
     return {"value": w.num_tokens * K / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K,
             "note": "host-synchronous per step, L2 not flushed; KV cache resident in HBM"}
+
+
+def e2e_pipelined_measure(db, w, dev, stream, K):
+    """The e2e step with the host link overlapped: two sets of per-step
+    device buffers; step k's inputs are copied in on one stream while step
+    k - 1 decodes, and step k - 1's results are copied out on a third stream
+    while step k decodes.  Every step still moves its own query, block table
+    and lengths in and its output and lse out through pinned host memory; a
+    step's inputs travel as one copy and its results as one (the tensors are
+    views of one buffer each), and the host waits for every result copy (a
+    step's host buffers are reused two steps later, after their copy has
+    finished)."""
+    import torch
+    from paged_mla_decode_08_gb300 import binding as B
+
+    def packed(tensors, pinned):
+        """One byte buffer holding `tensors` back to back (256-byte aligned),
+        and views of it shaped like them."""
+        offs, n = [], 0
+        for t in tensors:
+            offs.append(n)
+            n += -(-(t.numel() * t.element_size()) // 256) * 256
+        buf = torch.empty(n, dtype=torch.uint8, device="cpu" if pinned else dev)
+        if pinned:
+            buf = buf.pin_memory()
+        views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, tensors)]
+        return buf, views
+
+    ins = (db.q_nope, db.q_pe, db.block_table, db.seq_lens)
+    outs = (db.out, db.lse)
+    h_in, d_in, h_out, d_out = [], [], [], []
+    for _ in range(2):
+        hb, hv = packed(ins, True)
+        for v, t in zip(hv, ins):
+            v.copy_(t.cpu())
+        h_in.append((hb, hv))
+        d_in.append(packed(ins, False))
+        h_out.append(packed(outs, True))
+        d_out.append(packed(outs, False))
+    ws = [torch.empty_like(db.workspace) for _ in range(2)]
+    h2d = int(h_in[0][0].numel())
+    d2h = int(h_out[0][0].numel())
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_dec = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def run(n):
+        for k in range(n):
+            i = k & 1
+            if k >= 2:
+                ev_out[i].synchronize()  # the host has step k - 2's results; its buffers are free
+                s_in.wait_event(ev_dec[i])  # step k - 2 no longer reads set i
+            with torch.cuda.stream(s_in):
+                d_in[i][0].copy_(h_in[i][0], non_blocking=True)
+            ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            q, qp, bt, sl = d_in[i][1]
+            o, l = d_out[i][1]
+            B.mla_decode(db.plan, q, qp, db.kv, db.kv_dtype, bt, sl, w.scale, w.k_scale, o, l, ws[i], None, stream)
+            ev_dec[i].record(stream)
+            s_out.wait_event(ev_dec[i])
+            with torch.cuda.stream(s_out):
+                h_out[i][0].copy_(d_out[i][0], non_blocking=True)
+            ev_out[i].record(s_out)
+        for i in range(2):
+            ev_out[i].synchronize()
+
+    run(4)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    run(K)
+    el = time.perf_counter() - t0
+    last = h_out[(K - 1) & 1][1][0]
+    same = bool(torch.equal(last.view(torch.int16).to(dev), db.out.view(torch.int16)))
+    return {"value": w.num_tokens * K / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K, "result_matches_device_decode": same,
+            "note": "copies of step k+1 in and step k-1 out overlap the decode of step k (three streams; "
+                    "one copy each way per step); L2 not flushed; KV cache resident in HBM"}
 
 
 def main():
