@@ -323,6 +323,7 @@ def our_arm(args, w, rank, world):
     # host-synchronous per step, and with the host link overlapped
     e2e_serial = e2e_measure(db, w, dev, stream, max(3, min(K, 200)))
     e2e = e2e_pipelined_measure(db, w, dev, stream, max(3, min(K, 200)))
+    e2e_hio = e2e_host_io_measure(db, w, dev, stream, max(3, min(K, 200)))
     # ---- the step before the decode: block-table construction, timed alone
     bt_rows = block_table_measure(w, dev, stream, flush, max(3, min(K, 200)))
     # ---- ragged query counts (draft extend), the same decode kernels
@@ -368,6 +369,7 @@ def our_arm(args, w, rank, world):
                                    f"{cpu_rows} query tokens in {cpu_el:.1f} s"},
         "e2e": e2e,
         "e2e_serial": e2e_serial,
+        "e2e_host_io": e2e_hio,
         "gpu_launches": launches_per_step * K,
         "clocks": clocks,
         "kv_gbs": st["kv_bytes"] / step_avg_s / 1e9,
@@ -815,6 +817,55 @@ def e2e_pipelined_measure(db, w, dev, stream, K):
             "d2h_bytes_per_step": d2h, "steps": K, "result_matches_device_decode": same,
             "note": "copies of step k+1 in and step k-1 out overlap the decode of step k (three streams; "
                     "one copy each way per step); L2 not flushed; KV cache resident in HBM"}
+
+
+def e2e_host_io_measure(db, w, dev, stream, K):
+    """The e2e step through mla_decode_host_io, the call that takes the step's
+    inputs from host memory and returns its results there: two sets of
+    buffers (pinned host and device) on two streams, alternating, so one
+    step's copies overlap the other's decode.  Every step still moves its own
+    query, block table and lengths in and its output and lse out; the host
+    waits for a step's results before reusing its buffers two steps later."""
+    import torch
+    from paged_mla_decode_08_gb300 import binding as B
+    ins = (db.q_nope, db.q_pe, db.block_table, db.seq_lens)
+    outs = (db.out, db.lse)
+    h_in = [[t.cpu().pin_memory() for t in ins] for _ in range(2)]
+    h_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs] for _ in range(2)]
+    d_in = [[torch.empty_like(t) for t in ins] for _ in range(2)]
+    d_out = [[torch.empty_like(t) for t in outs] for _ in range(2)]
+    ws = [torch.empty_like(db.workspace) for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in[0])
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def run(n):
+        for k in range(n):
+            i = k & 1
+            if k >= 2:
+                done[i].synchronize()  # the host holds step k - 2's results; set i is free
+            q, qp, bt, sl = d_in[i]
+            o, l = d_out[i]
+            hq, hqp, hbt, hsl = h_in[i]
+            ho, hl = h_out[i]
+            B.mla_decode_host_io(db.plan, q, qp, db.kv, db.kv_dtype, bt, sl, w.scale, w.k_scale, o, l, ws[i],
+                                 hq, hqp, hbt, hsl, ho, hl, streams[i])
+            done[i].record(streams[i])
+        for e in done:
+            e.synchronize()
+
+    run(4)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    run(K)
+    el = time.perf_counter() - t0
+    same = bool(torch.equal(h_out[(K - 1) & 1][0].view(torch.int16).to(dev), db.out.view(torch.int16)))
+    return {"value": w.num_tokens * K / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K, "result_matches_device_decode": same,
+            "call": "mla_decode_host_io",
+            "note": "two buffer sets on two streams, alternating: one step's copies overlap the other's "
+                    "decode; L2 not flushed; KV cache resident in HBM"}
 
 
 def main():

@@ -151,6 +151,37 @@ int mla_decode(const mla_plan* plan, const void* q_nope, const void* q_pe, int n
                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * mla_decode for a caller whose per-step inputs and results live in host
+ * memory (a serving loop that receives the new query on the host): on
+ * `stream`, copy the step's inputs in, decode, and copy the results out.
+ *
+ *   q_nope_host, q_pe_host, block_table_host, seq_lens_host
+ *                 host arrays shaped like q_nope, q_pe, block_table and
+ *                 seq_lens of mla_decode; each is copied whole (one
+ *                 cudaMemcpyAsync each) into the device buffer of the same
+ *                 name, which this call therefore overwrites.
+ *   out_host, lse_host
+ *                 host arrays shaped like out and lse; the device results
+ *                 are copied there after the decode.
+ *   the rest      as for mla_decode (all device buffers).
+ *
+ * Returns once the work is queued: the host arrays must stay valid until the
+ * stream has passed them, and the results are in out_host / lse_host only
+ * after the caller synchronises with the stream (an event, say).  Pinned
+ * host memory (cudaHostAlloc) lets the copies run asynchronously, so that
+ * calls on two streams with two sets of buffers overlap one step's copies
+ * with another step's decode; pageable memory works but the copies then
+ * block the host.  Errors: those of mla_decode, MLA_ERR_ARG for a NULL host
+ * pointer, MLA_ERR_CUDA when a copy cannot be queued.
+ */
+int mla_decode_host_io(const mla_plan* plan, void* q_nope, void* q_pe, int num_tokens, int num_heads,
+                       const void* kv_pages, int kv_dtype, int64_t num_pages, int page_size,
+                       int32_t* block_table, int bt_stride, int32_t* seq_lens, float scale, float k_scale,
+                       void* out, float* lse, void* workspace, size_t workspace_bytes,
+                       const void* q_nope_host, const void* q_pe_host, const int32_t* block_table_host,
+                       const int32_t* seq_lens_host, void* out_host, float* lse_host, void* stream);
+
+/*
  * The two launches of mla_decode, exposed separately so callers (and the
  * benchmark) can time or interleave them.  mla_decode == mla_decode_main
  * followed by mla_decode_combine on the same stream, with the same

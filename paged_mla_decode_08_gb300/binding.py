@@ -37,6 +37,7 @@ SIGNATURES = {
     "mla_decode_main": (_c_int, _DECODE_ARGS),
     "mla_decode_combine": (_c_int, [_vp, _vp, _vp, _vp, _c_size, _vp]),
     "mla_decode_noalloc": (_c_int, _DECODE_ARGS[:16] + [_vp]),
+    "mla_decode_host_io": (_c_int, _DECODE_ARGS[:18] + [_vp] * 6 + [_vp]),
     "mla_decode_plan_ragged": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_vp),
                                         ctypes.POINTER(_c_size)]),
     "mla_decode_ragged": (_c_int, _DECODE_ARGS[:12] + [_vp] + _DECODE_ARGS[12:]),
@@ -216,6 +217,19 @@ def mla_decode(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_table, s
     """Decode into ``out`` / ``lse`` (torch CUDA tensors) on ``stream``."""
     _check(load().mla_decode(*_decode_args(plan, q_nope, q_pe, kv_pages, kv_dtype, block_table, seq_lens,
                                            scale, k_scale, out, lse, workspace, workspace_bytes, stream)))
+
+
+def mla_decode_host_io(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_table, seq_lens, scale: float,
+                       k_scale: float, out, lse, workspace, q_nope_host, q_pe_host, block_table_host, seq_lens_host,
+                       out_host, lse_host, stream=None):
+    """``mla_decode`` with the step's inputs copied in from, and its results
+    copied out to, host tensors (pinned for asynchronous copies); the device
+    tensors q_nope, q_pe, block_table and seq_lens are overwritten.  The host
+    results are valid once ``stream`` has been synchronised."""
+    args = _decode_args(plan, q_nope, q_pe, kv_pages, kv_dtype, block_table, seq_lens, scale, k_scale, out, lse,
+                        workspace, None, stream)
+    _check(load().mla_decode_host_io(*args[:18], _ptr(q_nope_host), _ptr(q_pe_host), _ptr(block_table_host),
+                                     _ptr(seq_lens_host), _ptr(out_host), _ptr(lse_host), args[18]))
 
 
 def mla_decode_ragged(plan: Plan, q_nope, q_pe, kv_pages, kv_dtype: int, block_table, seq_lens, cu_seqlens_q,

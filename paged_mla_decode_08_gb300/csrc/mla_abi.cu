@@ -252,6 +252,45 @@ int mla_decode(const mla_plan* plan, const void* q_nope, const void* q_pe, int n
   return rc == MLA_OK ? ok() : rc;
 }
 
+int mla_decode_host_io(const mla_plan* plan, void* q_nope, void* q_pe, int num_tokens, int num_heads,
+                       const void* kv_pages, int kv_dtype, int64_t num_pages, int page_size,
+                       int32_t* block_table, int bt_stride, int32_t* seq_lens, float scale, float k_scale,
+                       void* out, float* lse, void* workspace, size_t workspace_bytes,
+                       const void* q_nope_host, const void* q_pe_host, const int32_t* block_table_host,
+                       const int32_t* seq_lens_host, void* out_host, float* lse_host, void* stream) {
+  if (!q_nope_host || !q_pe_host || !block_table_host || !seq_lens_host || !out_host || !lse_host)
+    return fail(MLA_ERR_ARG, "a host pointer is NULL");
+  Prepared pr;
+  int rc = prepare(plan, q_nope, q_pe, num_tokens, num_heads, kv_pages, kv_dtype, num_pages, page_size,
+                   block_table, bt_stride, seq_lens, nullptr, scale, k_scale, out, lse, workspace, workspace_bytes,
+                   &pr);
+  if (rc != MLA_OK) return rc;
+  rc = check_device(nullptr);
+  if (rc != MLA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rows = (size_t)num_tokens * num_heads;
+  const size_t batch = (size_t)plan->batch;
+  struct Copy { void* dst; const void* src; size_t bytes; };
+  const Copy in[4] = {{q_nope, q_nope_host, rows * mla::kLatent * 2},
+                      {q_pe, q_pe_host, rows * mla::kRope * 2},
+                      {block_table, block_table_host, batch * (size_t)bt_stride * 4},
+                      {seq_lens, seq_lens_host, batch * 4}};
+  for (const Copy& cp : in) {
+    const cudaError_t e = cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("input copy: ") + cudaGetErrorString(e));
+  }
+  rc = launch_main(plan, pr, s);
+  if (rc != MLA_OK) return rc;
+  rc = launch_combine(plan, pr, s);
+  if (rc != MLA_OK) return rc;
+  const Copy res[2] = {{out_host, out, rows * mla::kLatent * 2}, {lse_host, lse, rows * 4}};
+  for (const Copy& cp : res) {
+    const cudaError_t e = cudaMemcpyAsync(cp.dst, cp.src, cp.bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return fail(MLA_ERR_CUDA, std::string("result copy: ") + cudaGetErrorString(e));
+  }
+  return ok();
+}
+
 int mla_decode_plan_ragged(const int32_t* seq_lens_host, const int32_t* q_lens_host, int batch, int page_size,
                            int num_heads, int num_sms, mla_plan** plan_out, size_t* workspace_bytes_out) {
   if (!plan_out) return fail(MLA_ERR_ARG, "plan_out is NULL");

@@ -84,6 +84,36 @@ def test_decode_rejects(split_plan, over, code):
     assert B.load().mla_decode_last_error_string()
 
 
+def call_host_io(plan, host_null=None, **over):
+    kw = dict(q_nope=FAKE, q_pe=FAKE, num_tokens=plan.batch * plan.q_len, num_heads=plan.num_heads,
+              kv=FAKE, kv_dtype=B.MLA_KV_BF16, num_pages=100, page_size=plan.page_size, bt=FAKE,
+              bt_stride=64, seq_lens=FAKE, scale=0.07, k_scale=1.0, out=FAKE, lse=FAKE,
+              ws=FAKE, ws_bytes=plan.workspace_bytes)
+    kw.update(over)
+    host = [FAKE] * 6
+    if host_null is not None:
+        host[host_null] = None
+    return B.load().mla_decode_host_io(plan.handle, kw["q_nope"], kw["q_pe"], kw["num_tokens"], kw["num_heads"],
+                                       kw["kv"], kw["kv_dtype"], kw["num_pages"], kw["page_size"], kw["bt"],
+                                       kw["bt_stride"], kw["seq_lens"], kw["scale"], kw["k_scale"], kw["out"],
+                                       kw["lse"], kw["ws"], kw["ws_bytes"], *host, None)
+
+
+@pytest.mark.parametrize("host_null", range(6))
+def test_host_io_rejects_null_host_pointer(split_plan, host_null):
+    assert call_host_io(split_plan, host_null) == B.MLA_ERR_ARG
+    assert "host pointer" in B.load().mla_decode_last_error_string().decode()
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(num_tokens=5), B.MLA_ERR_PLAN_MISMATCH),
+    (dict(q_nope=None), B.MLA_ERR_ARG),
+    (dict(ws=None), B.MLA_ERR_WORKSPACE),
+])
+def test_host_io_checks_device_arguments_like_decode(split_plan, over, code):
+    assert call_host_io(split_plan, **over) == code
+
+
 def test_decode_null_plan():
     rc = B.load().mla_decode(None, FAKE, FAKE, 1, 1, FAKE, 0, 1, 64, FAKE, 1, FAKE, 0.1, 1.0, FAKE, FAKE,
                              None, 0, None)
