@@ -24,10 +24,11 @@
 // written by the peer CTA.
 //
 // Warp roles (512 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer, warps 4-11 softmax / correction / epilogue (two warps per query
-// row block = TMEM lane quadrant, each owning half of a tile's keys and half
-// of the output columns), warps 12-15 score exchange with the peer CTA,
-// warps 2-3 e4m3 -> fp16 converters (float8 cache only).  Every wait is
+// MMA issuer (S products; with a bf16 cache warp 3 issues the P.V products),
+// warps 4-11 softmax / correction / epilogue (two warps per query row block =
+// TMEM lane quadrant, each owning half of a tile's keys and half of the
+// output columns), warps 12-15 score exchange with the peer CTA, warps 2-3
+// e4m3 -> fp16 converters (float8 cache only).  Every wait is
 // bounded: on timeout the kernel records an error code in device memory,
 // stops every role, waits for its own copies and MMAs, frees TMEM and
 // returns.
@@ -105,7 +106,8 @@ enum Bar : int {
   B_S_FREE = B_S_LOADED + 2,  // [tile parity]: softmax warps too; the S buffer may take the next S
   B_F8_FULL = B_S_FREE + 2,   // [fp8 stage]: TMA delivered the raw e4m3 tile
   B_F8_EMPTY = B_F8_FULL + kStages,  // [fp8 stage]: converted, may be refilled
-  B_COUNT = B_F8_EMPTY + kStages
+  B_FINAL2 = B_F8_EMPTY + kStages,  // the P.V issuer's own drain (two-issuer role split)
+  B_COUNT = B_FINAL2 + 1
 };
 constexpr int OFF_TMEM_SLOT = OFF_BAR + B_COUNT * 8;
 constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
@@ -479,13 +481,19 @@ __device__ void converter(const Ctx& c, const S& sched, const DecodeArgs& a, int
 // ------------------------------------------------------------------ MMA issuer
 
 template <class S, bool F8>
-__device__ void mma_issuer(const Ctx& c, const S& sched, const DecodeArgs& a, uint32_t tmem, int worker) {
+__device__ void mma_issuer(const Ctx& c, const S& sched, const DecodeArgs& a, uint32_t tmem, int worker, int role) {
   constexpr int NS = op_stages<F8>();
   constexpr uint32_t kIdescS = idesc_s<F8>(), kIdescPV = idesc_pv<F8>();
   // Two cursors walk this worker's tile sequence: S products run ahead as
   // soon as a cache tile has landed and the S buffer they write was read by
-  // the softmax warps; P.V products follow as P tiles appear.  Whichever is
-  // ready is issued, so S of tile j+2 never waits for P.V of tile j.
+  // the softmax warps; P.V products follow as P tiles appear.  role 0 issues
+  // both from this thread (whichever is ready), role 1 only the S products
+  // and role 2 only the P.V products, from two threads of different warps:
+  // issuing the 18 MMAs of an S product takes a single thread about 0.6 us,
+  // and a P tile that became ready meanwhile would wait for it.  The two
+  // streams touch disjoint TMEM (S buffers; O) and only read the cache stage;
+  // a stage is released after its P.V, which follows its S product (the
+  // softmax read that S before forming P).
   const int seg_end = sched.end(worker);
   auto first_live = [&](int s) {
     while (s < seg_end && segment_tiles(sched.seg(s), seg_len(c, sched, a, s)) == 0) ++s;
@@ -496,9 +504,9 @@ __device__ void mma_issuer(const Ctx& c, const S& sched, const DecodeArgs& a, ui
   int s_nt = s_seg < seg_end ? segment_tiles(sched.seg(s_seg), seg_len(c, sched, a, s_seg)) : 0;
   int p_nt = s_nt;
   long long t_last = clock64();
-  while (p_seg < seg_end) {
+  while (role == 1 ? s_seg < seg_end : p_seg < seg_end) {
     bool progressed = false;
-    if (s_seg < seg_end) {
+    if (role != 2 && s_seg < seg_end) {
       const int stage = s_j % NS;
       bool ready = (s_jj > 0 || mbar_test_wait(c.bar(B_Q_READY), q_used & 1)) &&
                    mbar_test_wait(c.bar(B_KV_FULL + stage), (s_j / NS) & 1) &&
@@ -530,7 +538,7 @@ __device__ void mma_issuer(const Ctx& c, const S& sched, const DecodeArgs& a, ui
         progressed = true;
       }
     }
-    if (p_j < s_j && mbar_test_wait(c.bar(B_P_FULL), p_j & 1)) {
+    if (role != 1 && (role == 2 || p_j < s_j) && mbar_test_wait(c.bar(B_P_FULL), p_j & 1)) {
       tc_fence_after();
       const uint32_t stage_addr = c.sbase + OFF_KV + (p_j % NS) * kStageBytes;
       const uint32_t p_addr = c.sbase + OFF_P;
@@ -564,9 +572,10 @@ __device__ void mma_issuer(const Ctx& c, const S& sched, const DecodeArgs& a, ui
     }
   }
   // all issued tensor-core work must finish before TMEM is released
-  mma_commit(c.bar(B_FINAL));
+  const uint32_t fin = c.bar(role == 2 ? B_FINAL2 : B_FINAL);
+  mma_commit(fin);
   const long long t0 = clock64();
-  while (!mbar_try_wait(c.bar(B_FINAL), 0) && clock64() - t0 < kTimeoutCycles) {
+  while (!mbar_try_wait(fin, 0) && clock64() - t0 < kTimeoutCycles) {
   }
 }
 
@@ -1024,7 +1033,10 @@ __device__ __forceinline__ void run_roles(const Ctx& c, const R& sched, const De
   if (warp == 0) {
     producer<R, F8, Q8>(c, sched, a, &tm_lat, &tm_rope, worker, rank);
   } else if (warp == 1) {
-    if ((threadIdx.x & 31) == 0) mma_issuer<R, F8>(c, sched, a, tmem, worker);
+    if ((threadIdx.x & 31) == 0) mma_issuer<R, F8>(c, sched, a, tmem, worker, F8 ? 0 : 1);
+    __syncwarp();
+  } else if (!F8 && warp == 3) {
+    if ((threadIdx.x & 31) == 0) mma_issuer<R, F8>(c, sched, a, tmem, worker, 2);
     __syncwarp();
   } else if (warp >= 12) {
     exchanger<R, F8, Q8>(c, sched, a, tmem, worker, rank);
@@ -1087,6 +1099,7 @@ __device__ __forceinline__ void decode_body(const S& sched, const DecodeArgs& a,
     mbar_init(c.bar(B_Q_READY), 128);
     mbar_init(c.bar(B_TAIL), 1);
     mbar_init(c.bar(B_FINAL), 1);
+    mbar_init(c.bar(B_FINAL2), 1);
     for (int i = 0; i < 8; ++i) mbar_init(c.bar(B_PAIR_MAX + i), 64);
     // receive buffers are armed one phase ahead: phase 0 now, phase u+1 as
     // soon as phase u completed (so the peer's bytes never precede the arm)
