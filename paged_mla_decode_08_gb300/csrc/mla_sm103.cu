@@ -832,18 +832,24 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
         if (!wait_bar_warp<false>(c, c.bar(B_S_LOADED + sb), (j >> 1) & 1, 0x301)) { ok = false; break; }
         tc_fence_after();
         uint32_t cur[32];
-        tmem_ld32(tmem + lane_off + TM_S + 64 * sb + 32 * half, cur);
-        tc_fence_before();
-        mbar_arrive(c.bar(B_S_FREE + sb));  // the MMA may overwrite this S buffer
+        // issued now, completed after the peer's half is read: the two latencies overlap
+        tmem_ld32_async(tmem + lane_off + TM_S + 64 * sb + 32 * half, cur);
         // ---- full scores: own partial + the peer's (its st.async bytes
         // complete the transaction count armed for this phase).  Re-arming
         // the next phase right away is safe: the peer cannot send into this
         // slot again before all "read" notes of this phase reached it.
         const int g = 2 * j + half, slot = g % kSlots, ug = g / kSlots;
-        if (warp_live && !wait_bar_warp<true>(c, c.bar(B_X_FULL + slot), ug & 1, 0x303)) { ok = false; break; }
+        if (warp_live && !wait_bar_warp<true>(c, c.bar(B_X_FULL + slot), ug & 1, 0x303)) {
+          tmem_wait_ld32(cur);
+          ok = false;
+          break;
+        }
         if (threadIdx.x == rearm_thread) mbar_arrive_expect_tx(c.bar(B_X_FULL + slot), kXchgRowBytes * M);  // row 0: live
         float x[32];
         if (!warp_live) {
+          tmem_wait_ld32(cur);
+          tc_fence_before();
+          mbar_arrive(c.bar(B_S_FREE + sb));  // the MMA may overwrite this S buffer
 #pragma unroll
           for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(cur[k]);  // masked below: no visible key
         } else {
@@ -854,6 +860,9 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
             const uint4 v = ld_shared_v4(srcx + ch * 2048);
             w[4 * ch + 0] = v.x; w[4 * ch + 1] = v.y; w[4 * ch + 2] = v.z; w[4 * ch + 3] = v.w;
           }
+          tmem_wait_ld32(cur);
+          tc_fence_before();
+          mbar_arrive(c.bar(B_S_FREE + sb));  // the MMA may overwrite this S buffer
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             float pv[4];
