@@ -31,7 +31,10 @@
 // e4m3 -> fp16 converters (float8 cache only).  Every wait is
 // bounded: on timeout the kernel records an error code in device memory,
 // stops every role, waits for its own copies and MMAs, frees TMEM and
-// returns.
+// returns.  The one hardware barrier, a quadrant's named barrier for the
+// per-tile row maxima, is released by a softmax warp that leaves early: it
+// arrives twice, enough for the furthest its partner can get before it
+// sees the abort.
 //
 // Float8 (e4m3) cache.  The same kernel, instantiated with F8 = true: TMA
 // brings raw e4m3 tiles (half the bytes) into a 2-stage fp8 ring, the two
@@ -100,8 +103,8 @@ constexpr int OFF_BAR = OFF_SEGS + kSegLenCache * 16;
 enum Bar : int {
   B_KV_FULL = 0, B_KV_EMPTY = B_KV_FULL + kStages, B_S_FULL = B_KV_EMPTY + kStages, B_P_FULL = B_S_FULL + 2,
   B_PV_DONE, B_Q_READY, B_X_FULL, B_X_EMPTY = B_X_FULL + kSlots, B_TAIL = B_X_EMPTY + kSlots, B_FINAL,
-  B_PAIR_MAX,                 // [quad][tile parity]: the two warps of a quadrant swap row maxima
-  B_PAIR_L = B_PAIR_MAX + 8,  // [quad]: ... and row sums at a segment's end
+  B_PAIR_L,                   // [quad]: the two warps of a quadrant swap row sums at a segment's end
+                              // (their per-tile row maxima go through named barriers 1-4)
   B_S_LOADED = B_PAIR_L + 4,  // [tile parity]: exchange warps hold S in registers
   B_S_FREE = B_S_LOADED + 2,  // [tile parity]: softmax warps too; the S buffer may take the next S
   B_F8_FULL = B_S_FREE + 2,   // [fp8 stage]: TMA delivered the raw e4m3 tile
@@ -808,6 +811,12 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
   const float cs = a.score_scale_log2;  // raw score -> base-2 logit
   int j = 0, nseg = 0;
   bool ok = true;
+  // leaving early: release the quadrant's other warp from the named barrier
+  // it may be waiting at, now or one tile later
+  auto bail = [&]() {
+    named_bar_arrive(1 + quad, 64);
+    named_bar_arrive(1 + quad, 64);
+  };
 
   for (int s = sched.begin(worker); ok && s < sched.end(worker); ++s) {
     const Segment sg = sched.seg(s);
@@ -829,7 +838,7 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
         const int sb = j & 1;
         // ---- own partial scores: the exchange warps have read S out of
         // TMEM (so P may overwrite it later); this thread's 32 columns
-        if (!wait_bar_warp<false>(c, c.bar(B_S_LOADED + sb), (j >> 1) & 1, 0x301)) { ok = false; break; }
+        if (!wait_bar_warp<false>(c, c.bar(B_S_LOADED + sb), (j >> 1) & 1, 0x301)) { ok = false; bail(); break; }
         tc_fence_after();
         uint32_t cur[32];
         // issued now, completed after the peer's half is read: the two latencies overlap
@@ -842,6 +851,7 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
         if (warp_live && !wait_bar_warp<true>(c, c.bar(B_X_FULL + slot), ug & 1, 0x303)) {
           tmem_wait_ld32(cur);
           ok = false;
+          bail();
           break;
         }
         if (threadIdx.x == rearm_thread) mbar_arrive_expect_tx(c.bar(B_X_FULL + slot), kXchgRowBytes * M);  // row 0: live
@@ -893,8 +903,7 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
         // row max) depends on every word read from the buffer
         if (valid_row) st_async_b32(sink_peer + slot * kNoteBytes, __float_as_uint(mt), x_empty_peer + 8 * slot);
         red_max[(sb * 2 + half) * 128 + row] = mt;
-        mbar_arrive(c.bar(B_PAIR_MAX + 2 * quad + sb));
-        if (!wait_bar_warp<false>(c, c.bar(B_PAIR_MAX + 2 * quad + sb), (j >> 1) & 1, 0x306)) { ok = false; break; }
+        named_bar_sync(1 + quad, 64);  // the quadrant's two warps swap row maxima (hardware barrier 1 + quad)
         mt = fmaxf(red_max[(sb * 2) * 128 + row], red_max[(sb * 2 + 1) * 128 + row]) * cs;
         // lazy rescale: the reference max moves only when it grew by more than
         // 2^8; both halves decide identically.  The decision and P need only
@@ -927,7 +936,7 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
         // ---- O and the P buffer are idle once the previous tile's P.V is
         // done; a rescale of O is TMEM traffic by whole warps
         if (jj > 0) {
-          if (!wait_bar_warp<false>(c, c.bar(B_PV_DONE), (j - 1) & 1, 0x304)) { ok = false; break; }
+          if (!wait_bar_warp<false>(c, c.bar(B_PV_DONE), (j - 1) & 1, 0x304)) { ok = false; bail(); break; }
           tc_fence_after();
           if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
@@ -955,7 +964,7 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
         mbar_arrive(c.bar(B_P_FULL));
       }
       if (!ok) break;
-      if (!wait_bar_warp<false>(c, c.bar(B_PV_DONE), (j - 1) & 1, 0x305)) { ok = false; break; }
+      if (!wait_bar_warp<false>(c, c.bar(B_PV_DONE), (j - 1) & 1, 0x305)) { ok = false; bail(); break; }
       tc_fence_after();
     }
 
@@ -966,7 +975,7 @@ __device__ void softmax_epilogue(const Ctx& c, const S& sched, const DecodeArgs&
       float* rl = red_l + (nseg & 1) * 256;
       rl[half * 128 + row] = l;
       mbar_arrive(c.bar(B_PAIR_L + quad));
-      if (!wait_bar_warp<false>(c, c.bar(B_PAIR_L + quad), nseg & 1, 0x307)) { ok = false; break; }
+      if (!wait_bar_warp<false>(c, c.bar(B_PAIR_L + quad), nseg & 1, 0x307)) { ok = false; bail(); break; }
       l = rl[row] + rl[128 + row];
       ++nseg;
     }
@@ -1109,7 +1118,6 @@ __device__ __forceinline__ void decode_body(const S& sched, const DecodeArgs& a,
     mbar_init(c.bar(B_TAIL), 1);
     mbar_init(c.bar(B_FINAL), 1);
     mbar_init(c.bar(B_FINAL2), 1);
-    for (int i = 0; i < 8; ++i) mbar_init(c.bar(B_PAIR_MAX + i), 64);
     // receive buffers are armed one phase ahead: phase 0 now, phase u+1 as
     // soon as phase u completed (so the peer's bytes never precede the arm)
     for (int k = 0; k < kSlots; ++k) mbar_arrive_expect_tx(c.bar(B_X_FULL + k), kXchgRowBytes * a.rows);
