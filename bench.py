@@ -740,16 +740,22 @@ def e2e_measure(db, w, dev, stream, K):
             "note": "host-synchronous per step, L2 not flushed; KV cache resident in HBM"}
 
 
-def e2e_pipelined_measure(db, w, dev, stream, K):
-    """The e2e step with the host link overlapped: two sets of per-step
-    device buffers; step k's inputs are copied in on one stream while step
-    k - 1 decodes, and step k - 1's results are copied out on a third stream
-    while step k decodes.  Every step still moves its own query, block table
-    and lengths in and its output and lse out through pinned host memory; a
+def e2e_pipelined_measure(db, w, dev, stream, K, sets=4):
+    """The e2e step with the host link overlapped: `sets` sets of per-step
+    buffers; step k's inputs are copied in on one stream while earlier steps
+    decode, and step k - 1's results are copied out on a third stream while
+    step k decodes.  Every step still moves its own query, block table and
+    lengths in and its output and lse out through pinned host memory; a
     step's inputs travel as one copy and its results as one (the tensors are
     views of one buffer each), and the host waits for every result copy (a
-    step's host buffers are reused two steps later, after their copy has
-    finished)."""
+    step's buffers are reused `sets` steps later, after the host has its
+    results).  The sets are independent batches in flight, as a server
+    interleaving micro-batches has them.  With two sets the host's wait for
+    step k - 2's results sits between step k - 1's decode and step k's copy
+    in, and the decode stalls on that chain (100 us a step on the
+    DeepSeek-V3-shaped batch); three sets give it one decode of slack (72.5
+    us) and four hide the copies entirely (69.4 us, against 70.9 us for the
+    decode alone while both copies run)."""
     import torch
     from paged_mla_decode_08_gb300 import binding as B
 
@@ -769,7 +775,7 @@ def e2e_pipelined_measure(db, w, dev, stream, K):
     ins = (db.q_nope, db.q_pe, db.block_table, db.seq_lens)
     outs = (db.out, db.lse)
     h_in, d_in, h_out, d_out = [], [], [], []
-    for _ in range(2):
+    for _ in range(sets):
         hb, hv = packed(ins, True)
         for v, t in zip(hv, ins):
             v.copy_(t.cpu())
@@ -777,20 +783,20 @@ def e2e_pipelined_measure(db, w, dev, stream, K):
         d_in.append(packed(ins, False))
         h_out.append(packed(outs, True))
         d_out.append(packed(outs, False))
-    ws = [torch.empty_like(db.workspace) for _ in range(2)]
+    ws = [torch.empty_like(db.workspace) for _ in range(sets)]
     h2d = int(h_in[0][0].numel())
     d2h = int(h_out[0][0].numel())
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_dec = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(sets)]
+    ev_dec = [torch.cuda.Event() for _ in range(sets)]
+    ev_out = [torch.cuda.Event() for _ in range(sets)]
 
     def run(n):
         for k in range(n):
-            i = k & 1
-            if k >= 2:
-                ev_out[i].synchronize()  # the host has step k - 2's results; its buffers are free
-                s_in.wait_event(ev_dec[i])  # step k - 2 no longer reads set i
+            i = k % sets
+            if k >= sets:
+                ev_out[i].synchronize()  # the host has step k - sets's results; its buffers are free
+                s_in.wait_event(ev_dec[i])  # step k - sets no longer reads set i
             with torch.cuda.stream(s_in):
                 d_in[i][0].copy_(h_in[i][0], non_blocking=True)
             ev_in[i].record(s_in)
@@ -803,48 +809,50 @@ def e2e_pipelined_measure(db, w, dev, stream, K):
             with torch.cuda.stream(s_out):
                 h_out[i][0].copy_(d_out[i][0], non_blocking=True)
             ev_out[i].record(s_out)
-        for i in range(2):
-            ev_out[i].synchronize()
+        for e in ev_out:
+            e.synchronize()
 
-    run(4)
+    run(2 * sets)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     run(K)
     el = time.perf_counter() - t0
-    last = h_out[(K - 1) & 1][1][0]
+    last = h_out[(K - 1) % sets][1][0]
     same = bool(torch.equal(last.view(torch.int16).to(dev), db.out.view(torch.int16)))
     return {"value": w.num_tokens * K / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": K, "result_matches_device_decode": same,
-            "note": "copies of step k+1 in and step k-1 out overlap the decode of step k (three streams; "
-                    "one copy each way per step); L2 not flushed; KV cache resident in HBM"}
+            "d2h_bytes_per_step": d2h, "steps": K, "result_matches_device_decode": same, "buffer_sets": sets,
+            "note": f"copies of later steps in and step k-1 out overlap the decode of step k (three streams; "
+                    f"{sets} buffer sets = {sets} independent batches in flight; one copy each way per step); "
+                    f"L2 not flushed (the 191 MB KV stream exceeds it); KV cache resident in HBM"}
 
 
-def e2e_host_io_measure(db, w, dev, stream, K):
+def e2e_host_io_measure(db, w, dev, stream, K, sets=4):
     """The e2e step through mla_decode_host_io, the call that takes the step's
-    inputs from host memory and returns its results there: two sets of
-    buffers (pinned host and device) on two streams, alternating, so one
-    step's copies overlap the other's decode.  Every step still moves its own
-    query, block table and lengths in and its output and lse out; the host
-    waits for a step's results before reusing its buffers two steps later."""
+    inputs from host memory and returns its results there: `sets` sets of
+    buffers (pinned host and device) on as many streams, in turn, so one
+    step's copies overlap the other steps' decodes.  Every step still moves
+    its own query, block table and lengths in and its output and lse out;
+    the host waits for a step's results before reusing its buffers `sets`
+    steps later."""
     import torch
     from paged_mla_decode_08_gb300 import binding as B
     ins = (db.q_nope, db.q_pe, db.block_table, db.seq_lens)
     outs = (db.out, db.lse)
-    h_in = [[t.cpu().pin_memory() for t in ins] for _ in range(2)]
-    h_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs] for _ in range(2)]
-    d_in = [[torch.empty_like(t) for t in ins] for _ in range(2)]
-    d_out = [[torch.empty_like(t) for t in outs] for _ in range(2)]
-    ws = [torch.empty_like(db.workspace) for _ in range(2)]
+    h_in = [[t.cpu().pin_memory() for t in ins] for _ in range(sets)]
+    h_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs] for _ in range(sets)]
+    d_in = [[torch.empty_like(t) for t in ins] for _ in range(sets)]
+    d_out = [[torch.empty_like(t) for t in outs] for _ in range(sets)]
+    ws = [torch.empty_like(db.workspace) for _ in range(sets)]
     h2d = sum(t.numel() * t.element_size() for t in h_in[0])
     d2h = sum(t.numel() * t.element_size() for t in h_out[0])
-    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
-    done = [torch.cuda.Event(), torch.cuda.Event()]
+    streams = [torch.cuda.Stream(device=dev) for _ in range(sets)]
+    done = [torch.cuda.Event() for _ in range(sets)]
 
     def run(n):
         for k in range(n):
-            i = k & 1
-            if k >= 2:
-                done[i].synchronize()  # the host holds step k - 2's results; set i is free
+            i = k % sets
+            if k >= sets:
+                done[i].synchronize()  # the host holds step k - sets's results; set i is free
             q, qp, bt, sl = d_in[i]
             o, l = d_out[i]
             hq, hqp, hbt, hsl = h_in[i]
@@ -855,17 +863,17 @@ def e2e_host_io_measure(db, w, dev, stream, K):
         for e in done:
             e.synchronize()
 
-    run(4)
+    run(2 * sets)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     run(K)
     el = time.perf_counter() - t0
-    same = bool(torch.equal(h_out[(K - 1) & 1][0].view(torch.int16).to(dev), db.out.view(torch.int16)))
+    same = bool(torch.equal(h_out[(K - 1) % sets][0].view(torch.int16).to(dev), db.out.view(torch.int16)))
     return {"value": w.num_tokens * K / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K, "result_matches_device_decode": same,
-            "call": "mla_decode_host_io",
-            "note": "two buffer sets on two streams, alternating: one step's copies overlap the other's "
-                    "decode; L2 not flushed; KV cache resident in HBM"}
+            "call": "mla_decode_host_io", "buffer_sets": sets,
+            "note": f"{sets} buffer sets on {sets} streams, in turn: one step's copies overlap the other "
+                    f"steps' decodes; L2 not flushed; KV cache resident in HBM"}
 
 
 def main():
