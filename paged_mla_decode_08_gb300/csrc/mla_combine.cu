@@ -14,12 +14,15 @@
 // of 8 output columns), so that the producing kernel stores coalesced.  One
 // CTA of 256 threads per (job, block of 32 query rows, quarter of the 64
 // chunks): a warp owns 2 chunks and reads them for 32 consecutive rows (512
-// contiguous bytes per chunk and split); the partials of the first 4, 8 or 16
+// contiguous bytes per chunk and split).  A launch whose widest job has more
+// than 8 splits gives each CTA a sixteenth of the row instead (128 threads, a
+// chunk per warp), so a request split 40 ways is merged by 64 CTAs per 128
+// rows, not 16.  The partials of the first 4, 8 or 16
 // splits (a group sized for the widest job of the launch) are requested
 // before the split weights e^{lse_s - lse} are computed (one warp, into
 // shared memory), so both memory latencies overlap, and later groups are
 // loaded one round each; the
-// 32 x 128 bf16 result is transposed through shared memory so that each
+// 32-row result is transposed through shared memory so that each
 // output row segment is written with contiguous 16-byte stores.  The bf16
 // partials add one rounding of O_s (relative 2^-9) before the merge, well
 // inside the output tolerance, and halve the bytes written and read.
@@ -45,37 +48,48 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return d;
 }
 
-// One (job, 32-row block, quarter of the columns) of the merge; called after
+// One (job, 32-row block, 1/kParts of the columns) of the merge; called after
 // the grid dependency wait.  kGroup splits' partials are in flight at a time:
 // the merge is a chain of dependent load rounds (ceil(nsplit / kGroup) of
-// them), so requests split many ways take a wider group.
-template <int kGroup>
-__device__ __forceinline__ void combine_body(const CombineJob job, const DecodeArgs& a, int row_block, int quarter) {
+// them), so requests split many ways take a wider group and more CTAs per
+// row block: kParts = 4 gives a CTA 16 chunks (8 warps, two chunks each),
+// kParts = 16 gives it 4 (4 warps, one chunk each).
+template <int kParts>
+__host__ __device__ constexpr int comb_threads() { return kParts == 4 ? 256 : 32 * (kChunks / kParts); }
+// column split of a launch whose widest job has more than 8 splits
+constexpr int kWideParts = 16;
+template <int kGroup, int kParts>
+__device__ __forceinline__ void combine_body(const CombineJob job, const DecodeArgs& a, int row_block, int part) {
+  static_assert(kParts == 4 || kParts == 16 || kParts == 32 || kParts == 64, "column split");
+  constexpr int kCtaChunks = kChunks / kParts;
+  constexpr int kWarps = comb_threads<kParts>() / 32;
+  constexpr int kPerWarp = kCtaChunks / kWarps;  // a warp's chunks: c0 + warp + kWarps * k
   extern __shared__ float s_w[];  // [nsplit][32] weights (0 for -inf splits)
   const int M = a.rows;  // partial-row stride: the planned rows per request
   const int r0 = row_block * kCombRows;
-  const int c0 = quarter * kCombChunks;
+  const int c0 = part * kCtaChunks;
   // this request's query rows (fewer than M in a ragged batch) and where
   // they go in out / lse
   const int2 q = request_q(a, job.req);
   const int nrows = min(kCombRows, q.y * a.num_heads - r0);
   if (nrows <= 0) return;  // whole CTA: no row of this block belongs to the request
   const size_t orow0 = (size_t)q.x * a.num_heads + r0;
-  __shared__ uint4 s_out[kCombRows][kCombChunks + 1];
+  __shared__ uint4 s_out[kCombRows][kCtaChunks + 1];
 
   const int r = threadIdx.x & 31;  // row within the block
-  const int cw = threadIdx.x >> 5;  // warp: chunks c0 + cw + 8k, k < 2
+  const int cw = threadIdx.x >> 5;  // warp
   const uint4* po = reinterpret_cast<const uint4*>(a.part_o) + ((size_t)job.slot_begin * kChunks + c0 + cw) * M + r0 + r;
   const size_t split_stride = (size_t)kChunks * M;
   // The partials of the first kGroup splits do not depend on the weights:
   // their loads go out before the lse values are even read, so the two
   // memory round trips overlap.
-  uint4 v[kGroup][2];
+  uint4 v[kGroup][kPerWarp];
 #pragma unroll
   for (int g = 0; g < kGroup; ++g)
 #pragma unroll
-    for (int k = 0; k < 2; ++k)
-      v[g][k] = (r < nrows && g < job.nsplit) ? __ldg(po + g * split_stride + (size_t)(8 * k) * M) : make_uint4(0, 0, 0, 0);
+    for (int k = 0; k < kPerWarp; ++k)
+      v[g][k] = (r < nrows && g < job.nsplit) ? __ldg(po + g * split_stride + (size_t)(kWarps * k) * M)
+                                              : make_uint4(0, 0, 0, 0);
 
   if (threadIdx.x < kCombRows) {
     // A split with lse = NaN (a NaN score in its keys) makes the row NaN, as
@@ -97,9 +111,9 @@ __device__ __forceinline__ void combine_body(const CombineJob job, const DecodeA
   }
   __syncthreads();
 
-  float acc[2][8];
+  float acc[kPerWarp][8];
 #pragma unroll
-  for (int k = 0; k < 2; ++k)
+  for (int k = 0; k < kPerWarp; ++k)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[k][e] = 0.f;
   if (r < nrows) {
@@ -108,8 +122,8 @@ __device__ __forceinline__ void combine_body(const CombineJob job, const DecodeA
 #pragma unroll
         for (int g = 0; g < kGroup; ++g)
 #pragma unroll
-          for (int k = 0; k < 2; ++k)
-            v[g][k] = s0 + g < job.nsplit ? __ldg(po + (s0 + g) * split_stride + (size_t)(8 * k) * M)
+          for (int k = 0; k < kPerWarp; ++k)
+            v[g][k] = s0 + g < job.nsplit ? __ldg(po + (s0 + g) * split_stride + (size_t)(kWarps * k) * M)
                                           : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
@@ -119,7 +133,7 @@ __device__ __forceinline__ void combine_body(const CombineJob job, const DecodeA
         const float wgt = s0 + g < job.nsplit ? s_w[(s0 + g) * kCombRows + r] : 0.f;
         if (wgt == 0.f) continue;
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < kPerWarp; ++k) {
           const uint32_t w4[4] = {v[g][k].x, v[g][k].y, v[g][k].z, v[g][k].w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -131,22 +145,24 @@ __device__ __forceinline__ void combine_body(const CombineJob job, const DecodeA
     }
   }
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < kPerWarp; ++k) {
     uint32_t q[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       __nv_bfloat162 h = __floats2bfloat162_rn(acc[k][2 * e], acc[k][2 * e + 1]);
       q[e] = *reinterpret_cast<uint32_t*>(&h);
     }
-    s_out[r][cw + 8 * k] = make_uint4(q[0], q[1], q[2], q[3]);
+    s_out[r][cw + kWarps * k] = make_uint4(q[0], q[1], q[2], q[3]);
   }
   __syncthreads();
-  // 32 rows x 256 bytes: a half-warp writes one row segment (16 lanes x 16 B)
-  const int hw = threadIdx.x >> 4, l16 = threadIdx.x & 15;
-  for (int rr = hw; rr < nrows; rr += 16) {
+  // 32 rows x kCtaChunks 16-byte chunks: kCtaChunks consecutive threads write
+  // one row segment with contiguous 16-byte stores
+  constexpr int kRowsPerPass = comb_threads<kParts>() / kCtaChunks;
+  const int lc = threadIdx.x % kCtaChunks;
+  for (int rr = threadIdx.x / kCtaChunks; rr < nrows; rr += kRowsPerPass) {
     const size_t row = orow0 + rr;
-    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * kLatent + kChunkCols * c0) + l16;
-    *dst = s_out[rr][l16];
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * kLatent + kChunkCols * c0) + lc;
+    *dst = s_out[rr][lc];
   }
 }
 
@@ -154,11 +170,11 @@ __device__ __forceinline__ void combine_body(const CombineJob job, const DecodeA
 // overlaps the main kernel's tail; the partials are read after the wait
 // (which returns once the main grid has completed and its writes are
 // visible; without the launch attribute it returns at once).
-template <int CAP, int kGroup>
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineList<CAP> jobs,
-                                                      const __grid_constant__ DecodeArgs a) {
+template <int CAP, int kGroup, int kParts>
+__global__ void __launch_bounds__(comb_threads<kParts>()) combine_kernel(const __grid_constant__ CombineList<CAP> jobs,
+                                                                       const __grid_constant__ DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  combine_body<kGroup>(jobs.job[blockIdx.x], a, blockIdx.y, blockIdx.z);
+  combine_body<kGroup, kParts>(jobs.job[blockIdx.x], a, blockIdx.y, blockIdx.z);
 }
 
 // Device plan: the job list is in the workspace, written by the planner
@@ -170,8 +186,8 @@ __global__ void __launch_bounds__(256) combine_kernel_dev(const CombineList<kJob
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if ((int)blockIdx.x >= __ldcg(&jobs->num_jobs)) return;
   const CombineJob* j = &jobs->job[blockIdx.x];  // 4-byte loads: no alignment assumed
-  combine_body<4>(CombineJob{__ldcg(&j->req), __ldcg(&j->slot_begin), __ldcg(&j->nsplit), 0}, a, blockIdx.y,
-                  blockIdx.z);
+  combine_body<4, 4>(CombineJob{__ldcg(&j->req), __ldcg(&j->slot_begin), __ldcg(&j->nsplit), 0}, a, blockIdx.y,
+                     blockIdx.z);
 }
 
 template <int CAP>
@@ -183,10 +199,12 @@ static cudaError_t launch_combine_cap(const std::vector<CombineJob>& jobs, const
   int maxsplit = 1;
   for (const CombineJob& j : jobs) maxsplit = j.nsplit > maxsplit ? j.nsplit : maxsplit;
   const size_t smem = (size_t)maxsplit * kCombRows * sizeof(float);  // <= 128 splits: 16 KB
+  // splits in flight per load round: enough for the widest job, within
+  // reason; more than 8 splits: a sixteenth of the row per CTA
+  const int parts = maxsplit <= 8 ? 4 : kWideParts;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)jobs.size(), (unsigned)((a.rows + kCombRows - 1) / kCombRows),
-                     (unsigned)(kChunks / kCombChunks));
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3((unsigned)jobs.size(), (unsigned)((a.rows + kCombRows - 1) / kCombRows), (unsigned)parts);
+  cfg.blockDim = dim3(parts == 4 ? comb_threads<4>() : comb_threads<kWideParts>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   // programmatic dependent launch: the grid may start while the main kernel
@@ -196,10 +214,9 @@ static cudaError_t launch_combine_cap(const std::vector<CombineJob>& jobs, const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // splits in flight per load round: enough for the widest job, within reason
-  if (maxsplit <= 4) return cudaLaunchKernelEx(&cfg, combine_kernel<CAP, 4>, list, a);
-  if (maxsplit <= 8) return cudaLaunchKernelEx(&cfg, combine_kernel<CAP, 8>, list, a);
-  return cudaLaunchKernelEx(&cfg, combine_kernel<CAP, 16>, list, a);
+  if (maxsplit <= 4) return cudaLaunchKernelEx(&cfg, combine_kernel<CAP, 4, 4>, list, a);
+  if (maxsplit <= 8) return cudaLaunchKernelEx(&cfg, combine_kernel<CAP, 8, 4>, list, a);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<CAP, 16, kWideParts>, list, a);
 }
 
 cudaError_t launch_combine(const std::vector<CombineJob>& jobs, const DecodeArgs& a,

@@ -358,7 +358,9 @@ def test_spike_keys_force_rescales(kv_dtype):
 ])
 def test_combine_group_sizes(lens, widest):
     """The combine loads the partials of 4, 8 or 16 splits per round, chosen
-    for the widest split of the launch; each width merges like the oracle."""
+    for the widest split of the launch (past 8 splits a CTA also takes a
+    sixteenth of the row instead of a quarter); each width merges like the
+    oracle."""
     w = W.make_workload("dsv3", seed=25, seq_lens=lens)
     db, out, lse = run_gpu(w)
     segs = db.plan.segments()
