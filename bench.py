@@ -448,7 +448,8 @@ def config_measure(name, seed, dev, stream, flush, K, peaks, peaks_kind):
         "workload": workload_desc(w)["workload"], "tokens_per_s": st["tokens"] / step_s,
         "step_us": step_s * 1e6, "main_us": main_s * 1e6, "combine_us": comb_us,
         "kv_gbs": st["kv_bytes"] / step_s / 1e9, "tflops": st["flops"] / step_s / 1e12,
-        "roofline": roofline_of(st, main_s, peaks, peaks_kind, "bf16" if w.kv_dtype == "bf16" else "fp16"),
+        "roofline": dict(roofline_of(st, main_s, peaks, peaks_kind, "bf16" if w.kv_dtype == "bf16" else "fp16"),
+                         traffic=profiled_traffic(w.name)),
         "step_roofline_frac": roofline_of(st, step_s, peaks, peaks_kind)["frac"],
         "host_plan_us": host_plan_us(w), "segments": int(len(db.plan.segments())),
         "partial_slots": db.plan.num_partial_slots, "steps": K, "launches_per_step": 1 + (db.plan.num_partial_slots > 0),
